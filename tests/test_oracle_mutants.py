@@ -1,0 +1,63 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies the oracle's C source, plants one mistake by text
+substitution, compiles the copy on the CPU and checks that the hand-worked
+example or the linked-list simulator comparison rejects it.  Nothing here
+touches the real oracle or any GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+# Not listed: dropping the explicit "skip slots hit this step" from the victim
+# candidates is an equivalent change, because hit slots already carry this
+# step's stamp (the newest) and K <= S leaves enough older slots.
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "hs_oracle.c")
+
+MUTANTS = {
+    "tie_break_highest_slot": ("if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;",
+                               "if (x->slot != y->slot) return x->slot < y->slot ? 1 : -1;"),
+    "hits_do_not_refresh": ("if (hit[s]) stamp[s] = step;", "if (0) stamp[s] = step;"),
+    "victims_in_lru_order": ("qsort(victims, (size_t)nmiss, sizeof(int32_t), or_cmp_int);", ""),
+    "victims_descending": ("int32_t v = victims[i];", "int32_t v = victims[nmiss - 1 - i];"),
+    "evicted_token_kept": ("if (old >= 0) tok_slot[old] = -1;", "(void)old;"),
+    "fill_not_stamped": ("        stamp[v] = step;\n", "\n"),
+    "wrong_row_copied": ("host + (size_t)t * (size_t)R", "host + (size_t)v * (size_t)R"),
+    "duplicates_accepted": ("if (seen[t]) { err |= OR_E_DUP; continue; }", ""),
+    "range_off_by_one": ("t >= len || t >= C", "t > len || t >= C"),
+    "tail_offset_from_start": ("out[j] = S + t % T;", "out[j] = S + (t - cold);"),
+    "tail_counted_as_miss": ("            inplace += 1;\n", "\n"),
+    "stamp_plus_one": ("if (hit[s]) stamp[s] = step;", "if (hit[s]) stamp[s] = step + 1;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_mistake(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    path = tmp_path / ("mut_%s.c" % name)
+    path.write_text(src.replace(old, new))
+    so = tmp_path / ("libmut_%s.so" % name)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-w", str(path), "-o", str(so)],
+                   check=True)
+    # Run the pins in a child process: a planted mistake may also crash.
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import oracle\n"
+        "from test_oracle import check_golden, check_against_simulator\n"
+        "lib = oracle.load_library(%r)\n"
+        "try:\n"
+        "    check_golden(oracle, lib=lib)\n"
+        "    check_against_simulator(oracle, range(400), lib=lib)\n"
+        "except AssertionError:\n"
+        "    sys.exit(3)\n"
+        "sys.exit(0)\n" % (here, os.path.dirname(here), str(so)))
+    rc = subprocess.run([sys.executable, "-c", code], capture_output=True).returncode
+    assert rc != 0, "planted mistake %s passed every pin" % name
