@@ -1,0 +1,495 @@
+"""Benchmark of the HiSparse swap-in path on GB300.
+
+Metric: top-k resolves/sec (one resolve = one request's K indices for one
+layer at one decode step) and miss-row GB/s, against the host->device link
+peak measured in the same run.
+
+Default workload: 64 requests, 64K-token contexts, top_k 2048, a 4096-slot hot
+buffer per request backed by a 16x pinned host pool, 1152-byte KV rows; the
+top-k trace keeps 70 % of each step's indices and draws the rest from
+Zipf(1.1).  The 2048-slot buffer of the same trace is measured alongside
+(the blog's buffer-size comparison) unless --no-sweep.
+
+One bench step = one call of the whole path (miss detection, LRU victims,
+table update, row fetch) for all requests.  The first 10 trace steps (the
+empty-buffer start) are run untimed, then --warmup steps untimed, then
+--steps timed steps.  L2 is flushed (a 256 MiB write) before every timed step,
+outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain sequential implementation the
+CUDA path is checked against) on the host cores over the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PRIME_STEPS = 10
+METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _workload_desc(wl):
+    return ("%s: B=%d requests, ctx %d tokens, top_k %d, buffer %d slots, host pool %dx buffer, "
+            "resident tail %d, %d layer(s), row %d B, trace %d%% carry-over / %d%% Zipf(%.1f) / rest %s, "
+            "seed %d" % (wl.name, wl.B, wl.C, wl.K, wl.S, wl.host_ratio, wl.T, wl.layers,
+                         wl.row_bytes, wl.carry_pct, wl.zipf_pct, wl.zipf_a,
+                         ["Zipf", "uniform", "recent window %d" % wl.recent][wl.third], wl.seed))
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the measured region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str = None):
+        self.proc = None
+        self.lines = []
+        self.path = out_path
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if self.path:
+            with open(self.path, "w") as f:
+                f.write("sm_mhz,max_sm_mhz,power_w,active,hw_slowdown,hw_thermal,sw_thermal,sw_power_cap\n")
+                f.write(out)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[2] > 250.0] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------- peaks
+def measure_h2d_peak(torch, hs, nbytes=1 << 30, reps=5):
+    """Best of `reps` for a pinned->device cudaMemcpyAsync and for the zero-copy read kernel."""
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host.fill_(3)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best_ce = best_zc = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        e0.record()
+        dev.copy_(host, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        best_ce = min(best_ce, e0.elapsed_time(e1))
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        e0.record()
+        hs.hs_h2d_read(host.data_ptr(), dev.data_ptr(), nbytes, 0, torch.cuda.current_stream())
+        e1.record()
+        e1.synchronize()
+        best_zc = min(best_zc, e0.elapsed_time(e1))
+    ok = bool(torch.equal(dev[:4096].cpu(), host[:4096]))
+    del host, dev
+    ce = nbytes / best_ce / 1e6
+    zc = nbytes / best_zc / 1e6
+    return {"copy_engine_gbs": ce, "zero_copy_kernel_gbs": zc, "peak_gbs": max(ce, zc),
+            "zero_copy_checked": ok, "bytes": nbytes}
+
+
+def measure_hbm_peak(torch):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                v = float(json.load(f)["hbm_gbs"])
+            return v, "MEASURED_PEAKS.json hbm_gbs (measured copy on this pool)"
+        except (ValueError, KeyError, OSError):
+            pass
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(5):
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return 2 * n / best / 1e6, "device copy measured in this run (read + write bytes)"
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist):
+    import torch
+    from hierarchical_kv_cache_hs_gb300 import hs
+    from hierarchical_kv_cache_hs_gb300 import tracegen as tg
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+
+    wl = tg.WORKLOADS[args.workload]
+    total_steps = PRIME_STEPS + args.warmup + args.steps
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    peaks = measure_h2d_peak(torch, hs)
+    hbm_gbs, hbm_src = measure_hbm_peak(torch)
+
+    def measure(wl, want_profile=True, want_e2e=True):
+        w = GpuWorkload(wl, steps=total_steps, record=False, host_trace=want_e2e,
+                        request_offset=rank * wl.B)
+        stream = torch.cuda.Stream(device=dev)
+        res = {}
+        try:
+            def stats_sum(key):
+                return sum(hs.hs_stats(h.h)[key] for h in w.handles)
+
+            # --- device-resident timed pass -------------------------------
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            launches = 0
+            misses_per_step = []
+            with torch.cuda.stream(stream):
+                for s in range(PRIME_STEPS + args.warmup):
+                    w.launch_step(s, stream)
+                stream.synchronize()
+                m0 = stats_sum("misses")
+                barrier()
+                torch.cuda.synchronize()
+                t_wall0 = time.perf_counter()
+                for i in range(args.steps):
+                    s = PRIME_STEPS + args.warmup + i
+                    flush.fill_(i & 0xFF)
+                    starts[i].record(stream)
+                    launches += w.launch_step(s, stream)
+                    ends[i].record(stream)
+                torch.cuda.synchronize()
+                barrier()
+                t_wall = time.perf_counter() - t_wall0
+            step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+            dev_ms = sum(step_ms)
+            miss_rows = stats_sum("misses") - m0
+            res.update(dev_ms=dev_ms, step_ms=step_ms, wall_s=t_wall, launches=launches,
+                       miss_rows=miss_rows)
+
+            # --- per-step miss counts + copy-kernel durations (second pass) ----
+            if want_profile:
+                w.reset()
+                before = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+                after = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+                rs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+                copy_ms = []
+                resolve_ms = []
+                import numpy as np
+                last = np.zeros(wl.B, dtype=np.int32)
+                with torch.cuda.stream(stream):
+                    for s in range(PRIME_STEPS + args.warmup):
+                        w.launch_step(s, stream)
+                    for i in range(args.steps):
+                        s = PRIME_STEPS + args.warmup + i
+                        flush.fill_(i & 0xFF)
+                        tot = 0
+                        cms = rms = 0.0
+                        for layer, h in enumerate(w.handles):
+                            for e in (before[i], after[i], rs[i]):
+                                e.record(stream)
+                            hs.hs_profile_events(h.h, before[i], after[i])
+                            if w.append_rows is not None:
+                                hs.hs_append(h.h, w.append_rows[layer, s], stream)
+                            rs[i].record(stream)
+                            hs.hs_resolve(h.h, w.topk[layer, s], wl.K, w.out[layer], stream)
+                            hs.hs_profile_events(h.h, None, None)
+                            stream.synchronize()
+                            hs.hs_stats(h.h, last)
+                            tot += int(last.sum())
+                            cms += before[i].elapsed_time(after[i])
+                            rms += rs[i].elapsed_time(before[i])
+                        misses_per_step.append(tot)
+                        copy_ms.append(cms)
+                        resolve_ms.append(rms)
+                res.update(misses_per_step=misses_per_step, copy_ms=copy_ms, resolve_ms=resolve_ms)
+
+            # --- end to end through hs_resolve_host -----------------------
+            if want_e2e:
+                w.reset()
+                out_host = torch.empty((wl.layers, wl.B, wl.K), dtype=torch.int32).pin_memory()
+                with torch.cuda.stream(stream):
+                    for s in range(PRIME_STEPS + args.warmup):
+                        w.host_step(s, out_host, stream)
+                    e2e_s = 0.0
+                    for i in range(args.steps):
+                        s = PRIME_STEPS + args.warmup + i
+                        flush.fill_(i & 0xFF)
+                        stream.synchronize()
+                        t0 = time.perf_counter()
+                        w.host_step(s, out_host, stream)
+                        e2e_s += time.perf_counter() - t0
+                res.update(e2e_s=e2e_s)
+        finally:
+            w.close()
+        return res
+
+    sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    main = measure(wl)
+    clocks = sampler.stop()
+
+    sweep = {}
+    if not args.no_sweep and args.workload == "b64_c64k_s4096":
+        other = tg.WORKLOADS["b64_c64k_s2048"]
+        r2 = measure(other, want_profile=True, want_e2e=False)
+        sweep["b64_c64k_s2048"] = {
+            "resolves_per_s": other.B * other.layers * args.steps / (r2["dev_ms"] / 1e3),
+            "miss_row_gbs": r2["miss_rows"] * other.row_bytes / (r2["dev_ms"] / 1e3) / 1e9,
+            "ms_per_step": r2["dev_ms"] / args.steps,
+            "misses_per_step_mean": statistics.mean(r2["misses_per_step"]),
+            "misses_per_step": r2["misses_per_step"],
+        }
+
+    units = wl.B * wl.layers * args.steps
+    dev_s = max_over_ranks(main["dev_ms"] / 1e3)
+    all_units = sum_over_ranks(units)
+    value = all_units / dev_s
+    miss_bytes = main["miss_rows"] * wl.row_bytes
+    miss_gbs = sum_over_ranks(miss_bytes) / dev_s / 1e9
+    h2d_peak = peaks["peak_gbs"]
+
+    # Roofline of the dominant kernel (row copy): algorithmic bytes are the
+    # miss rows (R bytes each) read over the host link, per launch.
+    copy_s = sum(main["copy_ms"]) / 1e3
+    copy_gbs = (sum(main["misses_per_step"]) * wl.row_bytes) / copy_s / 1e9
+    # Whole-step roofline: max(miss bytes / H2D peak, table bytes / HBM peak).
+    t_roof = 0.0
+    for m in main["misses_per_step"]:
+        table = wl.layers * (wl.B * (16 * wl.K + 4 * wl.S)) + 16 * m
+        t_roof += max(m * wl.row_bytes / (h2d_peak * 1e9), table / (hbm_gbs * 1e9))
+    step_frac = t_roof / (main["dev_ms"] / 1e3)
+
+    e2e_value = all_units / max_over_ranks(main["e2e_s"])
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "resolves/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": main["dev_ms"] / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic (seeded top-k traces and uniform random KV row bytes)",
+        "config": {
+            "workload": _workload_desc(wl),
+            "prime_steps_untimed": PRIME_STEPS,
+            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+            "parallelism": "requests sharded over ranks, no collective on the data path",
+        },
+        "miss_row_gbs": miss_gbs,
+        "h2d_peak": peaks,
+        "miss_row_frac_of_h2d_peak": miss_gbs / h2d_peak,
+        "step_roofline": {"t_roof_ms_per_step": t_roof * 1e3 / args.steps,
+                          "frac": step_frac,
+                          "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
+                          "table_bytes_per_resolve": "16K + 4S + 16m"},
+        "roofline": {"bound": "h2d", "kernel": "hs_copy_kernel", "achieved": copy_gbs,
+                     "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
+                     "traffic": None,
+                     "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
+                                    "1 GiB zero-copy 128-bit read kernel)"},
+        "kernel_ms_per_step": {"copy": sum(main["copy_ms"]) / args.steps,
+                               "resolve": sum(main["resolve_ms"]) / args.steps},
+        "misses_per_step_mean": statistics.mean(main["misses_per_step"]),
+        "misses_per_step": main["misses_per_step"],
+        "e2e": {"value": e2e_value, "unit": "resolves/s",
+                "h2d_bytes_per_step": wl.layers * wl.B * wl.K * 4,
+                "d2h_bytes_per_step": wl.layers * wl.B * wl.K * 4,
+                "api": "hs_resolve_host (pinned host top-k in, host out_slot back, synchronised)"},
+        "gpu_launches": main["launches"],
+        "clocks": clocks,
+        "wall_s_timed_region": main["wall_s"],
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args, total_steps)
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_requests(wl, total_steps, requests, threads, time_from_step):
+    """Replay the trace on the CPU oracle; returns seconds spent on steps >= time_from_step."""
+    import numpy as np
+    import oracle
+    from hierarchical_kv_cache_hs_gb300 import tracegen as tg
+    trace = tg.topk_trace(wl, steps=total_steps, requests=requests)
+    hosts = {}
+
+    def prep(i):
+        b = requests[i]
+        hosts[i] = tg.rows(wl, 0, b, 0, wl.cold)
+
+    oracle.parallel_map(prep, range(len(requests)), threads)
+    states = [oracle.RequestState(wl.C, wl.S, wl.T, wl.row_bytes) for _ in requests]
+    from concurrent.futures import ThreadPoolExecutor
+
+    elapsed = 0.0
+    with ThreadPoolExecutor(threads) as ex:
+        for s in range(total_steps):
+            def run(i, s=s):
+                states[i].resolve(hosts[i], trace[s, i], s + 1)
+            t0 = time.perf_counter()
+            list(ex.map(run, range(len(requests))))
+            if s >= time_from_step:
+                elapsed += time.perf_counter() - t0
+    return elapsed
+
+
+def cpu_baseline(wl, args, total_steps):
+    """The oracle as it stands, over all requests, on every host core."""
+    cores = _cores()
+    if wl.layers != 1 or wl.grow:
+        return {"value": None, "unit": "resolves/s", "cores": cores, "kind": "oracle",
+                "sample": "not run for multi-layer / growing workloads"}
+    from_step = PRIME_STEPS + args.warmup
+    secs = _oracle_requests(wl, total_steps, list(range(wl.B)), cores, from_step)
+    n = wl.B * (total_steps - from_step)
+    return {"value": n / secs, "unit": "resolves/s", "cores": cores, "kind": "oracle",
+            "sample": "the timed steps of the same trace, all %d requests, one request per thread "
+                      "per step, after replaying the untimed prefix" % wl.B}
+
+
+def run_reference(args):
+    from hierarchical_kv_cache_hs_gb300 import tracegen as tg
+    wl = tg.WORKLOADS[args.workload]
+    total_steps = PRIME_STEPS + args.warmup + args.steps
+    cores = _cores()
+    secs = _oracle_requests(wl, total_steps, list(range(wl.B)), cores, PRIME_STEPS + args.warmup)
+    units = wl.B * wl.layers * args.steps
+    value = units / secs
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "resolves/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic (seeded top-k traces and uniform random KV row bytes)",
+        "config": {"workload": _workload_desc(wl), "prime_steps_untimed": PRIME_STEPS},
+        "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": cores, "kind": "oracle",
+                         "sample": "every timed step of the workload, all %d requests, one request "
+                                   "per thread" % wl.B},
+        "e2e": {"value": value, "unit": "resolves/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=180)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="b64_c64k_s4096")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    from hierarchical_kv_cache_hs_gb300 import build
+    if rank == 0:
+        build.build_all()
+    if dist is not None:
+        dist.barrier()
+    line = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,436 @@
+// Host side of the C ABI declared in include/hs.h: handle lifetime,
+// argument checks, launches and state export.  The host never reads device
+// data on the resolve path; everything it enqueues is graph-capturable.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "hs_internal.h"
+
+struct hs_handle {
+    int B, C, R, S, T, H, cold;
+    int device;
+    int32_t* d_tok_slot;   // [B][C]
+    int32_t* d_slot_tok;   // [B][S]
+    int32_t* d_stamp;      // [B][S]
+    int32_t* d_len;        // [B]
+    uint8_t* d_buf;        // [B][S+T][R]
+    uint8_t* h_pool;       // pinned, mapped [B][H][R]
+    uint8_t* d_pool;       // device address of h_pool
+    int32_t* d_miss_tok;   // [B][S] scratch: this step's miss tokens
+    int32_t* d_miss_slot;  // [B][S] scratch: their victim slots
+    int32_t* d_miss_cnt;   // [B]
+    HsDevState* d_st;
+    int32_t* d_stage_in;   // [B][min(S, HS_MAX_TOPK)] for hs_resolve_host
+    int32_t* d_stage_out;
+    cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
+    int copy_grid;
+    int copy_unroll;
+    int copy_rows_per_group;
+    size_t pool_bytes, buf_bytes;
+};
+
+namespace {
+
+// Switch to the handle's device for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool switched = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            switched = cudaSetDevice(dev) == cudaSuccess;
+        }
+    }
+    ~DeviceGuard()
+    {
+        if (switched) cudaSetDevice(prev);
+    }
+};
+
+template <class T>
+cudaError_t dalloc(T** p, size_t n)
+{
+    *p = nullptr;
+    if (n == 0) n = 1;
+    return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
+}
+
+void free_all(hs_handle* h)
+{
+    if (!h) return;
+    cudaFree(h->d_tok_slot);
+    cudaFree(h->d_slot_tok);
+    cudaFree(h->d_stamp);
+    cudaFree(h->d_len);
+    cudaFree(h->d_buf);
+    cudaFree(h->d_miss_tok);
+    cudaFree(h->d_miss_slot);
+    cudaFree(h->d_miss_cnt);
+    cudaFree(h->d_st);
+    cudaFree(h->d_stage_in);
+    cudaFree(h->d_stage_out);
+    if (h->h_pool) cudaFreeHost(h->h_pool);
+}
+
+int fill_start_state(hs_handle* h)
+{
+    const size_t B = (size_t)h->B;
+    if (cudaMemset(h->d_tok_slot, 0xff, B * h->C * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemset(h->d_slot_tok, 0xff, B * h->S * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemset(h->d_stamp, 0, B * h->S * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemset(h->d_miss_cnt, 0, B * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemset(h->d_st, 0, sizeof(HsDevState)) != cudaSuccess) return HS_ERR_CUDA;
+    std::vector<int32_t> len(B, h->C);
+    if (cudaMemcpy(h->d_len, len.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+// State reads and setup calls wait for all work on the device, so a stream
+// the caller has since destroyed is never touched.
+int sync_last(hs_handle*)
+{
+    return cudaDeviceSynchronize() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+bool valid(const hs_handle* h)
+{
+    return h != nullptr && h->B > 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hs_error_string(int code)
+{
+    switch (code) {
+    case HS_OK: return "ok";
+    case HS_ERR_ARG: return "invalid argument";
+    case HS_ERR_TOPK_GT_SLOTS: return "top-k larger than the buffer slots";
+    case HS_ERR_CAPACITY: return "host pool smaller than the host-backed context";
+    case HS_ERR_ALLOC: return "allocation failed";
+    case HS_ERR_CUDA: return "CUDA runtime error";
+    case HS_ERR_LIMIT: return "size beyond the kernel limits";
+    default: return "unknown error";
+    }
+}
+
+int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_ratio,
+              int resident_tail, hs_handle** out)
+{
+    if (!out) return HS_ERR_ARG;
+    *out = nullptr;
+    if (batch <= 0 || ctx_len <= 0 || row_bytes <= 0 || buffer_slots <= 0 || host_ratio <= 0 ||
+        resident_tail < 0 || resident_tail > ctx_len || (row_bytes % 16) != 0)
+        return HS_ERR_ARG;
+    if (batch > HS_MAX_BATCH || buffer_slots > HS_MAX_SLOTS || row_bytes > HS_MAX_ROW_BYTES)
+        return HS_ERR_LIMIT;
+    const long long H = (long long)host_ratio * buffer_slots;
+    if (H < (long long)ctx_len - resident_tail) return HS_ERR_CAPACITY;
+    if (H > 0x7fffffffLL) return HS_ERR_LIMIT;
+
+    hs_handle* h = new (std::nothrow) hs_handle();
+    if (!h) return HS_ERR_ALLOC;
+    h->B = batch;
+    h->C = ctx_len;
+    h->R = row_bytes;
+    h->S = buffer_slots;
+    h->T = resident_tail;
+    h->H = (int)H;
+    h->cold = ctx_len - resident_tail;
+    if (cudaGetDevice(&h->device) != cudaSuccess) {
+        delete h;
+        return HS_ERR_CUDA;
+    }
+
+    const size_t B = (size_t)batch;
+    const int kmax = buffer_slots < HS_MAX_TOPK ? buffer_slots : HS_MAX_TOPK;
+    h->pool_bytes = B * (size_t)h->H * (size_t)row_bytes;
+    h->buf_bytes = B * (size_t)(buffer_slots + resident_tail) * (size_t)row_bytes;
+    bool ok = dalloc(&h->d_tok_slot, B * ctx_len) == cudaSuccess &&
+              dalloc(&h->d_slot_tok, B * buffer_slots) == cudaSuccess &&
+              dalloc(&h->d_stamp, B * buffer_slots) == cudaSuccess &&
+              dalloc(&h->d_len, B) == cudaSuccess &&
+              dalloc(&h->d_buf, h->buf_bytes) == cudaSuccess &&
+              dalloc(&h->d_miss_tok, B * buffer_slots) == cudaSuccess &&
+              dalloc(&h->d_miss_slot, B * buffer_slots) == cudaSuccess &&
+              dalloc(&h->d_miss_cnt, B) == cudaSuccess &&
+              dalloc(&h->d_st, 1) == cudaSuccess &&
+              dalloc(&h->d_stage_in, B * kmax) == cudaSuccess &&
+              dalloc(&h->d_stage_out, B * kmax) == cudaSuccess;
+    if (ok) {
+        void* p = nullptr;
+        ok = cudaHostAlloc(&p, h->pool_bytes ? h->pool_bytes : 1, cudaHostAllocMapped) == cudaSuccess;
+        h->h_pool = static_cast<uint8_t*>(p);
+        if (ok) {
+            void* dp = nullptr;
+            ok = cudaHostGetDevicePointer(&dp, p, 0) == cudaSuccess;
+            h->d_pool = static_cast<uint8_t*>(dp);
+        }
+    }
+    if (!ok) {
+        cudaGetLastError();
+        free_all(h);
+        delete h;
+        return HS_ERR_ALLOC;
+    }
+    if (hs_prepare_resolve() != cudaSuccess) {
+        free_all(h);
+        delete h;
+        return HS_ERR_CUDA;
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (sms <= 0) sms = 1;
+    h->copy_unroll = hs_copy_unroll_for(row_bytes);
+    h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
+    h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
+    const int rc = fill_start_state(h);
+    if (rc != HS_OK) {
+        free_all(h);
+        delete h;
+        return rc;
+    }
+    *out = h;
+    return HS_OK;
+}
+
+void hs_destroy(hs_handle* h)
+{
+    if (!h) return;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    free_all(h);
+    h->B = 0;
+    delete h;
+}
+
+int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+               hs_stream_t stream)
+{
+    if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
+    if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    ResolveArgs ra;
+    ra.topk = topk_idx;
+    ra.out = out_slot;
+    ra.tok_slot = h->d_tok_slot;
+    ra.slot_tok = h->d_slot_tok;
+    ra.stamp = h->d_stamp;
+    ra.len = h->d_len;
+    ra.miss_tok = h->d_miss_tok;
+    ra.miss_slot = h->d_miss_slot;
+    ra.miss_cnt = h->d_miss_cnt;
+    ra.st = h->d_st;
+    ra.K = K;
+    ra.C = h->C;
+    ra.S = h->S;
+    ra.T = h->T;
+    ra.cold = h->cold;
+    ra.list_stride = h->S;
+    ra.hash_bits = hs_hash_bits(K);
+    if (hs_launch_resolve(ra, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
+
+    CopyArgs ca;
+    ca.miss_cnt = h->d_miss_cnt;
+    ca.miss_tok = h->d_miss_tok;
+    ca.miss_slot = h->d_miss_slot;
+    ca.pool = h->d_pool;
+    ca.buf = h->d_buf;
+    ca.st = h->d_st;
+    ca.B = h->B;
+    ca.S = h->S;
+    ca.T = h->T;
+    ca.R = h->R;
+    ca.list_stride = h->S;
+    ca.H = h->H;
+    ca.rows_per_group = h->copy_rows_per_group;
+    ca.advance_step = 1;
+    const bool prof = h->prof_before && h->prof_after;
+    if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
+    if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
+    if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                    hs_stream_t stream)
+{
+    if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
+    if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)h->B * (size_t)K * sizeof(int32_t);
+    if (cudaMemcpyAsync(h->d_stage_in, topk_idx, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    const int rc = hs_resolve(h, h->d_stage_in, K, h->d_stage_out, stream);
+    if (rc != HS_OK) return rc;
+    if (cudaMemcpyAsync(out_slot, h->d_stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_stats(hs_handle* h, hs_stats_t* out, int32_t* last_miss)
+{
+    if (!valid(h) || !out) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    HsDevState st;
+    if (cudaMemcpy(&st, h->d_st, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return HS_ERR_CUDA;
+    out->steps = st.step;
+    out->hits = (int64_t)st.hits;
+    out->misses = (int64_t)st.misses;
+    out->inplace = (int64_t)st.inplace;
+    out->bytes_copied = (int64_t)st.misses * h->R;
+    out->err_bits = st.err;
+    out->reserved = 0;
+    if (last_miss &&
+        cudaMemcpy(last_miss, h->d_miss_cnt, (size_t)h->B * sizeof(int32_t), cudaMemcpyDeviceToHost) !=
+            cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+uint8_t* hs_host_pool(hs_handle* h) { return valid(h) ? h->h_pool : nullptr; }
+size_t hs_host_pool_bytes(hs_handle* h) { return valid(h) ? h->pool_bytes : 0; }
+uint8_t* hs_device_buffer(hs_handle* h) { return valid(h) ? h->d_buf : nullptr; }
+size_t hs_device_buffer_bytes(hs_handle* h) { return valid(h) ? h->buf_bytes : 0; }
+
+int hs_set_lengths(hs_handle* h, const int32_t* len_host)
+{
+    if (!valid(h) || !len_host) return HS_ERR_ARG;
+    for (int b = 0; b < h->B; ++b)
+        if (len_host[b] < 0 || len_host[b] > h->C) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    if (cudaMemcpy(h->d_len, len_host, (size_t)h->B * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream)
+{
+    if (!valid(h) || !rows_dev || h->T <= 0) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    AppendArgs a;
+    a.rows = rows_dev;
+    a.buf = h->d_buf;
+    a.len = h->d_len;
+    a.st = h->d_st;
+    a.S = h->S;
+    a.T = h->T;
+    a.R = h->R;
+    a.C = h->C;
+    a.cold = h->cold;
+    if (hs_launch_append(a, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t* rows_host)
+{
+    if (!valid(h) || !rows_host || b < 0 || b >= h->B || n < 0 || h->T <= 0) return HS_ERR_ARG;
+    if (first_token < h->cold || (long long)first_token + n > h->C) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    const size_t R = (size_t)h->R;
+    uint8_t* base = h->d_buf + (size_t)b * (size_t)(h->S + h->T) * R;
+    // Consecutive tokens occupy consecutive tail slots until t mod T wraps.
+    for (int i = 0; i < n;) {
+        const int t = first_token + i;
+        const int slot = t % h->T;
+        int run = h->T - slot;
+        if (run > n - i) run = n - i;
+        if (cudaMemcpy(base + (size_t)(h->S + slot) * R, rows_host + (size_t)i * R, (size_t)run * R,
+                       cudaMemcpyHostToDevice) != cudaSuccess)
+            return HS_ERR_CUDA;
+        i += run;
+    }
+    return HS_OK;
+}
+
+int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp,
+                    int32_t* step)
+{
+    if (!valid(h)) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    const size_t B = (size_t)h->B;
+    if (tok_slot && cudaMemcpy(tok_slot, h->d_tok_slot, B * h->C * sizeof(int32_t),
+                               cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (slot_tok && cudaMemcpy(slot_tok, h->d_slot_tok, B * h->S * sizeof(int32_t),
+                               cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (stamp && cudaMemcpy(stamp, h->d_stamp, B * h->S * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (step) {
+        HsDevState st;
+        if (cudaMemcpy(&st, h->d_st, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return HS_ERR_CUDA;
+        *step = st.step;
+    }
+    return HS_OK;
+}
+
+int hs_export_buffer(hs_handle* h, int b, uint8_t* dst_host)
+{
+    if (!valid(h) || !dst_host || b < 0 || b >= h->B) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    const size_t row = (size_t)(h->S + h->T) * (size_t)h->R;
+    if (cudaMemcpy(dst_host, h->d_buf + (size_t)b * row, row, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_reset(hs_handle* h)
+{
+    if (!valid(h)) return HS_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    return fill_start_state(h);
+}
+
+int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy)
+{
+    if (!valid(h) || (before_copy == nullptr) != (after_copy == nullptr)) return HS_ERR_ARG;
+    h->prof_before = static_cast<cudaEvent_t>(before_copy);
+    h->prof_after = static_cast<cudaEvent_t>(after_copy);
+    return HS_OK;
+}
+
+int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks, hs_stream_t stream)
+{
+    if (!src_host || !dst_dev || bytes == 0 || (bytes % 16) != 0 || blocks < 0) return HS_ERR_ARG;
+    void* dsrc = nullptr;
+    if (cudaHostGetDevicePointer(&dsrc, const_cast<void*>(src_host), 0) != cudaSuccess) {
+        cudaGetLastError();
+        return HS_ERR_ARG;
+    }
+    int grid = blocks;
+    if (grid == 0) {
+        int dev = 0, sms = 1;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid = sms * 4;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hs_launch_h2d_read(static_cast<const uint8_t*>(dsrc), static_cast<uint8_t*>(dst_dev), bytes,
+                           grid, s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+}  // extern "C"

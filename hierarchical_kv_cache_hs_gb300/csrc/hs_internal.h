@@ -1,0 +1,76 @@
+// Private declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "hs.h"
+
+// Device-resident per-handle control word: the step counter, latched error
+// bits and cumulative counters.  The resolve kernel reads `step` (this call's
+// step is step + 1), the copy kernel that follows it advances `step`.
+struct HsDevState {
+    int32_t step;
+    int32_t err;
+    unsigned long long hits;
+    unsigned long long misses;
+    unsigned long long inplace;
+};
+
+struct ResolveArgs {
+    const int32_t* topk;   // [B][K]
+    int32_t* out;          // [B][K]
+    int32_t* tok_slot;     // [B][C]
+    int32_t* slot_tok;     // [B][S]
+    int32_t* stamp;        // [B][S]
+    const int32_t* len;    // [B]
+    int32_t* miss_tok;     // [B][list_stride]  miss tokens, top-k row order
+    int32_t* miss_slot;    // [B][list_stride]  their victim slots
+    int32_t* miss_cnt;     // [B]
+    HsDevState* st;
+    int K, C, S, T, cold;
+    int list_stride;
+    int hash_bits;         // dedup hash capacity = 1 << hash_bits >= 2K
+};
+
+struct CopyArgs {
+    const int32_t* miss_cnt;
+    const int32_t* miss_tok;
+    const int32_t* miss_slot;
+    const uint8_t* pool;   // device-usable address of the mapped pinned pool [B][H][R]
+    uint8_t* buf;          // [B][S+T][R]
+    HsDevState* st;
+    int B, S, T, R, list_stride;
+    long long H;
+    int rows_per_group;    // rows a warp copies together (its lanes < rows_per_group own one row each)
+    int advance_step;      // 1: block 0 advances st->step after the primary grid finished
+};
+
+struct AppendArgs {
+    const uint8_t* rows;   // [B][R]
+    uint8_t* buf;
+    int32_t* len;
+    HsDevState* st;
+    int S, T, R, C, cold;
+};
+
+// Resolve kernel launch geometry.
+constexpr int HS_RESOLVE_THREADS = 1024;
+constexpr int HS_COPY_THREADS = 256;
+
+size_t hs_resolve_smem_bytes(int K, int S);
+int hs_hash_bits(int K);
+cudaError_t hs_prepare_resolve();
+cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s);
+
+// Copy kernel: `pdl` lets it launch while the resolve grid drains (it waits
+// on the resolve grid's completion before reading the miss lists).
+cudaError_t hs_launch_copy(const CopyArgs& a, int grid, int unroll, cudaStream_t s, bool pdl);
+int hs_copy_unroll_for(int row_bytes);
+int hs_copy_rows_per_group(int row_bytes, int unroll);
+int hs_copy_blocks_per_sm(int unroll, int B);
+
+cudaError_t hs_launch_append(const AppendArgs& a, int B, cudaStream_t s);
+cudaError_t hs_launch_h2d_read(const uint8_t* src, uint8_t* dst, size_t bytes, int grid,
+                               cudaStream_t s);

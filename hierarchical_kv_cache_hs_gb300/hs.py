@@ -1,0 +1,275 @@
+"""Python binding of ``libhs.so`` (the C ABI in ``include/hs.h``).
+
+Argument marshalling only: every step of the swap-in path runs in the CUDA
+library.  Pointers may be given as integers, torch tensors (``data_ptr()``) or
+numpy arrays; streams as ``None`` (legacy default stream), an integer handle
+or a ``torch.cuda.Stream``.  Errors returned by the library raise ``HsError``.
+
+Importing this module loads the library and raises ``ImportError`` when it has
+not been built -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhs.so")
+
+HS_OK = 0
+HS_ERR_ARG = -1
+HS_ERR_TOPK_GT_SLOTS = -2
+HS_ERR_CAPACITY = -3
+HS_ERR_ALLOC = -4
+HS_ERR_CUDA = -5
+HS_ERR_LIMIT = -6
+
+HS_E_RANGE = 1
+HS_E_DUP = 2
+HS_E_APPEND = 4
+
+HS_MAX_TOPK = 4096
+HS_MAX_SLOTS = 16384
+HS_MAX_BATCH = 4096
+HS_MAX_ROW_BYTES = 65536
+
+
+class HsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (where, hs_error_string(code), code))
+
+
+class hs_stats_t(ctypes.Structure):
+    _fields_ = [
+        ("steps", ctypes.c_int64),
+        ("hits", ctypes.c_int64),
+        ("misses", ctypes.c_int64),
+        ("inplace", ctypes.c_int64),
+        ("bytes_copied", ctypes.c_int64),
+        ("err_bits", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libhs.so is not built (run __graft_entry__.build() or "
+                          "python -m hierarchical_kv_cache_hs_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "hs_create": ([I, I, I, I, I, I, ctypes.POINTER(P)], I),
+        "hs_destroy": ([P], None),
+        "hs_resolve": ([P, P, I, P, P], I),
+        "hs_resolve_host": ([P, P, I, P, P], I),
+        "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
+        "hs_host_pool": ([P], P),
+        "hs_host_pool_bytes": ([P], Z),
+        "hs_device_buffer": ([P], P),
+        "hs_device_buffer_bytes": ([P], Z),
+        "hs_set_lengths": ([P, P], I),
+        "hs_append": ([P, P, P], I),
+        "hs_set_tail_rows": ([P, I, I, I, P], I),
+        "hs_export_state": ([P, P, P, P, P], I),
+        "hs_export_buffer": ([P, I, P], I),
+        "hs_reset": ([P], I),
+        "hs_h2d_read": ([P, P, Z, I, P], I),
+        "hs_profile_events": ([P, P, P], I),
+        "hs_error_string": ([I], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError("cannot take a pointer of %r" % type(x))
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    raise TypeError("cannot take a stream handle of %r" % type(s))
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != HS_OK:
+        raise HsError(rc, where)
+
+
+def hs_error_string(code: int) -> str:
+    return lib.hs_error_string(int(code)).decode()
+
+
+def hs_create(batch: int, ctx_len: int, row_bytes: int, buffer_slots: int, host_ratio: int,
+              resident_tail: int = 0) -> int:
+    """Create a handle; returns its address.  Raises HsError on a library error."""
+    out = ctypes.c_void_p()
+    _check(lib.hs_create(batch, ctx_len, row_bytes, buffer_slots, host_ratio, resident_tail,
+                         ctypes.byref(out)), "hs_create")
+    return out.value
+
+
+def hs_create_rc(batch, ctx_len, row_bytes, buffer_slots, host_ratio, resident_tail=0):
+    """hs_create returning (code, handle) instead of raising."""
+    out = ctypes.c_void_p()
+    rc = lib.hs_create(batch, ctx_len, row_bytes, buffer_slots, host_ratio, resident_tail,
+                       ctypes.byref(out))
+    return rc, out.value
+
+
+def hs_destroy(h: int) -> None:
+    lib.hs_destroy(h)
+
+
+def hs_resolve(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
+    _check(lib.hs_resolve(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream)),
+           "hs_resolve")
+
+
+def hs_resolve_rc(h: int, topk_idx, K: int, out_slot, stream=None) -> int:
+    return lib.hs_resolve(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream))
+
+
+def hs_resolve_host(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
+    _check(lib.hs_resolve_host(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream)),
+           "hs_resolve_host")
+
+
+def hs_stats(h: int, last_miss=None) -> dict:
+    st = hs_stats_t()
+    _check(lib.hs_stats(h, ctypes.byref(st), _ptr(last_miss)), "hs_stats")
+    return {f: getattr(st, f) for f, _ in hs_stats_t._fields_ if f != "reserved"}
+
+
+def hs_host_pool(h: int) -> int:
+    return lib.hs_host_pool(h) or 0
+
+
+def hs_host_pool_bytes(h: int) -> int:
+    return int(lib.hs_host_pool_bytes(h))
+
+
+def hs_device_buffer(h: int) -> int:
+    return lib.hs_device_buffer(h) or 0
+
+
+def hs_device_buffer_bytes(h: int) -> int:
+    return int(lib.hs_device_buffer_bytes(h))
+
+
+def hs_set_lengths(h: int, lengths) -> None:
+    arr = np.ascontiguousarray(lengths, dtype=np.int32)
+    _check(lib.hs_set_lengths(h, arr.ctypes.data), "hs_set_lengths")
+
+
+def hs_append(h: int, rows_dev, stream=None) -> None:
+    _check(lib.hs_append(h, _ptr(rows_dev), _stream(stream)), "hs_append")
+
+
+def hs_set_tail_rows(h: int, b: int, first_token: int, rows_host: np.ndarray) -> None:
+    arr = np.ascontiguousarray(rows_host, dtype=np.uint8)
+    _check(lib.hs_set_tail_rows(h, int(b), int(first_token), int(arr.shape[0]), arr.ctypes.data),
+           "hs_set_tail_rows")
+
+
+def hs_export_state(h: int, tok_slot=None, slot_tok=None, stamp=None) -> int:
+    """Copy the tables into the given host arrays; returns the step counter."""
+    step = np.zeros(1, dtype=np.int32)
+    _check(lib.hs_export_state(h, _ptr(tok_slot), _ptr(slot_tok), _ptr(stamp), step.ctypes.data),
+           "hs_export_state")
+    return int(step[0])
+
+
+def hs_export_buffer(h: int, b: int, dst_host) -> None:
+    _check(lib.hs_export_buffer(h, int(b), _ptr(dst_host)), "hs_export_buffer")
+
+
+def hs_reset(h: int) -> None:
+    _check(lib.hs_reset(h), "hs_reset")
+
+
+def hs_h2d_read(src_host, dst_dev, nbytes: int, blocks: int = 0, stream=None) -> None:
+    _check(lib.hs_h2d_read(_ptr(src_host), _ptr(dst_dev), int(nbytes), int(blocks),
+                           _stream(stream)), "hs_h2d_read")
+
+
+def hs_profile_events(h: int, before_copy=None, after_copy=None) -> None:
+    """Record two CUDA events (torch.cuda.Event or raw handles) around the copy kernel."""
+    def ev(e):
+        if e is None:
+            return None
+        return e.cuda_event if hasattr(e, "cuda_event") else int(e)
+    _check(lib.hs_profile_events(h, ev(before_copy), ev(after_copy)), "hs_profile_events")
+
+
+class Handle:
+    """Owning wrapper: one swap-in state (one layer, B requests)."""
+
+    def __init__(self, batch, ctx_len, row_bytes, buffer_slots, host_ratio, resident_tail=0):
+        self.B, self.C, self.R, self.S = batch, ctx_len, row_bytes, buffer_slots
+        self.T, self.host_ratio = resident_tail, host_ratio
+        self.H = host_ratio * buffer_slots
+        self.h = hs_create(batch, ctx_len, row_bytes, buffer_slots, host_ratio, resident_tail)
+
+    def close(self):
+        if getattr(self, "h", None):
+            hs_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def host_pool(self) -> np.ndarray:
+        """The pinned host pool as a numpy view [B][H][R] (uint8)."""
+        n = hs_host_pool_bytes(self.h)
+        buf = (ctypes.c_uint8 * n).from_address(hs_host_pool(self.h))
+        return np.frombuffer(buf, dtype=np.uint8).reshape(self.B, self.H, self.R)
+
+    def resolve(self, topk_idx, K, out_slot, stream=None):
+        hs_resolve(self.h, topk_idx, K, out_slot, stream)
+
+    def stats(self, last_miss=None):
+        return hs_stats(self.h, last_miss)
+
+    def export_state(self):
+        tok = np.empty((self.B, self.C), dtype=np.int32)
+        st = np.empty((self.B, self.S), dtype=np.int32)
+        stamp = np.empty((self.B, self.S), dtype=np.int32)
+        step = hs_export_state(self.h, tok, st, stamp)
+        return tok, st, stamp, step
+
+    def export_buffer(self, b: int) -> np.ndarray:
+        out = np.empty((self.S + self.T, self.R), dtype=np.uint8)
+        hs_export_buffer(self.h, b, out)
+        return out

@@ -1,0 +1,121 @@
+"""Run a synthetic swap-in workload through the C ABI.
+
+Sets up one handle per layer, fills each pinned host pool with the seeded KV
+rows, writes the resident tail (fixed context) or uploads the per-step rows
+to append (growing context), and uploads the top-k trace to the device.
+Every resolve goes through ``hs_resolve`` / ``hs_append``; this file only
+prepares inputs and issues calls.  torch provides device memory and streams.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import hs
+from . import tracegen as tg
+
+
+class GpuWorkload:
+    """Handles, inputs and output buffers of one workload on one GPU.
+
+    ``steps`` decode steps of trace are generated (default: the workload's).
+    With ``record=True`` every step's out_slot is kept on the device
+    ([layers][steps][B][K]); otherwise one [layers][B][K] buffer is reused.
+    """
+
+    def __init__(self, wl: tg.Workload, steps: Optional[int] = None, record: bool = False,
+                 device: str = "cuda", threads: Optional[int] = None, host_trace: bool = False,
+                 request_offset: int = 0):
+        self.wl = wl
+        self.steps = wl.steps if steps is None else int(steps)
+        self.device = torch.device(device)
+        self.record = record
+        self.layers = wl.layers
+        B, K, R = wl.B, wl.K, wl.row_bytes
+        reqs = list(range(request_offset, request_offset + B))
+        self.handles = []
+        for layer in range(wl.layers):
+            h = hs.Handle(B, wl.C, R, wl.S, wl.host_ratio, wl.T)
+            self.handles.append(h)
+            # Cold rows of request b live at pool row t of request slot b.
+            self._fill_pool(h, layer, reqs, threads)
+            if wl.grow:
+                hs.hs_set_lengths(h.h, np.full(B, wl.len0, dtype=np.int32))
+            elif wl.T > 0:
+                for i, b in enumerate(reqs):
+                    rows = tg.rows(wl, layer, b, wl.cold, wl.T)
+                    hs.hs_set_tail_rows(h.h, i, wl.cold, rows)
+        # Top-k trace: [layers][steps][B][K] int32.
+        host = np.empty((wl.layers, self.steps, B, K), dtype=np.int32)
+        for layer in range(wl.layers):
+            tg.topk_trace(wl, layer=layer, steps=self.steps, requests=reqs, threads=threads,
+                          out=host[layer])
+        self.topk = torch.from_numpy(host).to(self.device)
+        self.topk_host = torch.from_numpy(host).pin_memory() if host_trace else None
+        # Rows appended before each step (growing context): [layers][steps][B][R].
+        self.append_rows = None
+        if wl.grow:
+            ap = np.empty((wl.layers, self.steps, B, R), dtype=np.uint8)
+            for layer in range(wl.layers):
+                for i, b in enumerate(reqs):
+                    ap[layer, :, i, :] = tg.rows(wl, layer, b, wl.len0, self.steps)
+            self.append_rows = torch.from_numpy(ap).to(self.device)
+        if record:
+            self.out = torch.full((wl.layers, self.steps, B, K), -7, dtype=torch.int32,
+                                  device=self.device)
+        else:
+            self.out = torch.full((wl.layers, B, K), -7, dtype=torch.int32, device=self.device)
+        self.requests = reqs
+
+    def _fill_pool(self, h, layer, reqs, threads):
+        wl = self.wl
+        base = hs.hs_host_pool(h.h)
+        R, H = wl.row_bytes, wl.H
+        # The generator keys rows by the request id; the pool is indexed by position.
+        from concurrent.futures import ThreadPoolExecutor
+        jobs = [(i, b, t0, min(4096, wl.cold - t0))
+                for i, b in enumerate(reqs) for t0 in range(0, wl.cold, 4096)]
+
+        def one(job):
+            i, b, t0, n = job
+            tg.fill_rows_ptr(wl, layer, b, t0, n, base + (i * H + t0) * R, R)
+
+        with ThreadPoolExecutor(tg._workers(threads)) as ex:
+            list(ex.map(one, jobs))
+
+    def out_at(self, layer: int, step: int) -> torch.Tensor:
+        return self.out[layer, step] if self.record else self.out[layer]
+
+    def launch_step(self, s: int, stream=None) -> int:
+        """Enqueue step s for every layer; returns the number of kernel launches."""
+        wl = self.wl
+        n = 0
+        for layer, h in enumerate(self.handles):
+            if self.append_rows is not None:
+                hs.hs_append(h.h, self.append_rows[layer, s], stream)
+                n += 1
+            hs.hs_resolve(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), stream)
+            n += 2
+        return n
+
+    def host_step(self, s: int, out_host: torch.Tensor, stream=None) -> None:
+        """Step s from host buffers (hs_resolve_host), for end-to-end timing."""
+        wl = self.wl
+        for layer, h in enumerate(self.handles):
+            if self.append_rows is not None:
+                hs.hs_append(h.h, self.append_rows[layer, s], stream)
+            hs.hs_resolve_host(h.h, self.topk_host[layer, s], wl.K, out_host[layer], stream)
+
+    def reset(self) -> None:
+        wl = self.wl
+        for h in self.handles:
+            hs.hs_reset(h.h)
+            if wl.grow:
+                hs.hs_set_lengths(h.h, np.full(wl.B, wl.len0, dtype=np.int32))
+
+    def close(self) -> None:
+        for h in self.handles:
+            h.close()
+        self.handles = []

@@ -1,0 +1,213 @@
+/*
+ * hs.h -- C ABI of the HiSparse swap-in path on one GB300 GPU.
+ *
+ * The operation (HiSparse blog, section "Efficient swap-in kernel"; the
+ * papercache summary of it, section 2 "Method", steps 1-3): for every request
+ * at every decode step, take the indexer's top-k token indices and
+ *   (1) find which of them miss in the request's hot device buffer,
+ *   (2) choose eviction victims by LRU among the slots not hit this step,
+ *   (3) update the token->slot page table, the slot->token table and the
+ *       per-slot last-use stamps, and fetch each missing KV row from the
+ *       pinned host pool into its victim slot.
+ * The result is a [B, K] list of buffer slots that a sparse-attention kernel
+ * reads.  With a resident tail (vLLM "Hybrid HiSparse" post, section "Mixed
+ * Residency"), tokens in the last T positions of the context live on the
+ * device and resolve in place; a request starts with an empty buffer (same
+ * post, "No Residency").
+ *
+ * Exact semantics (the library reproduces them bit for bit):
+ *   - one token per page; stamps hold the step of last use (steps count from
+ *     1, stamp 0 = never used); a hit refreshes its slot's stamp;
+ *   - victims are the m slots not hit this step with the smallest
+ *     (stamp, slot index) pairs -- ties go to the lowest slot index; the i-th
+ *     miss in top-k row order is paired with the i-th victim in ascending slot
+ *     order;
+ *   - a tail token t (C - T <= t < len) resolves to slot S + (t mod T) and
+ *     touches no table; it counts as neither hit nor miss;
+ *   - index -1 is padding (out = -1).  An index < -1 or >= the request's
+ *     current length, or a repeat of an earlier index in the same row, is a
+ *     device-side input error: out = -1 for that entry, the state is left as
+ *     if the entry were absent, and an error bit is latched (hs_stats).
+ *
+ * Layouts (row-major, all int32 unless stated):
+ *   topk_idx, out_slot         [B][K]
+ *   token->slot table          [B][C]        (-1 = not in the buffer)
+ *   slot->token table, stamps  [B][S]
+ *   device buffer (uint8)      [B][S + T][R] (slots [0,S) hot, [S,S+T) tail)
+ *   host pool (uint8, pinned and mapped)  [B][H][R], H = host_ratio * S,
+ *                              row t of request b holds token t (t < C - T)
+ *
+ * Ownership: the library allocates and frees everything in a handle (device
+ * tables, buffer, scratch, pinned host pool).  Pointers passed in by the
+ * caller stay the caller's and must remain valid until the stream reaches the
+ * work that uses them.  A handle is bound to the device that was current at
+ * hs_create; calls switch to that device and restore the caller's.
+ *
+ * Errors: host-side checks return a negative HS_ERR_* synchronously and
+ * enqueue nothing.  Device-side input errors never trap; they are latched in
+ * the handle's error word (HS_E_* bits, read by hs_stats).
+ *
+ * Streams: hs_stream_t is cudaStream_t (NULL = the legacy default stream).
+ * hs_resolve and hs_append only enqueue work (no host synchronisation, no
+ * allocation), so a sequence of them can be captured in a CUDA graph.
+ */
+#ifndef HS_H
+#define HS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hs_handle hs_handle;
+typedef struct CUstream_st* hs_stream_t;
+
+/* Return codes. */
+#define HS_OK                 0
+#define HS_ERR_ARG           -1  /* bad size, null pointer, or bad handle */
+#define HS_ERR_TOPK_GT_SLOTS -2  /* K > buffer_slots: the LRU step needs K <= S */
+#define HS_ERR_CAPACITY      -3  /* host pool too small: host_ratio * S < ctx_len - resident_tail */
+#define HS_ERR_ALLOC         -4  /* device or pinned host allocation failed */
+#define HS_ERR_CUDA          -5  /* a CUDA runtime call or launch failed */
+#define HS_ERR_LIMIT         -6  /* a size beyond the kernels' limits below */
+
+/* Device-side error bits (hs_stats_t.err_bits). */
+#define HS_E_RANGE   1  /* an index < -1 or >= the request's current length */
+#define HS_E_DUP     2  /* an index repeated within one top-k row */
+#define HS_E_APPEND  4  /* hs_append with no room in the resident tail */
+
+/* Kernel limits. */
+#define HS_MAX_TOPK       4096
+#define HS_MAX_SLOTS      16384
+#define HS_MAX_BATCH      4096
+#define HS_MAX_ROW_BYTES  65536
+
+typedef struct {
+    int64_t steps;         /* resolves issued on the handle (its step counter) */
+    int64_t hits;          /* cumulative buffer hits */
+    int64_t misses;        /* cumulative misses (= rows fetched from host) */
+    int64_t inplace;       /* cumulative resident-tail resolves */
+    int64_t bytes_copied;  /* misses * row_bytes */
+    int32_t err_bits;      /* HS_E_* latched since create / reset */
+    int32_t reserved;
+} hs_stats_t;
+
+/*
+ * Create the swap-in state for `batch` requests of one layer.
+ *   ctx_len        C, capacity in tokens (valid positions [0, C))
+ *   row_bytes      R, bytes per KV row; a multiple of 16
+ *   buffer_slots   S, hot-buffer slots per request (SGLang's device_buffer_size)
+ *   host_ratio     H = host_ratio * S host rows per request (SGLang's
+ *                  host_to_device_ratio); must cover C - resident_tail
+ *   resident_tail  T >= 0, device-resident tail tokens (0 = no mixed residency)
+ * All tables start empty, stamps 0, step 0, every request's length = C
+ * (use hs_set_lengths for a growing context).  The host pool is allocated
+ * but not filled: write the cold rows through hs_host_pool before resolving.
+ * Returns HS_OK and *out, or an HS_ERR_* code (then *out = NULL).
+ */
+int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_ratio,
+              int resident_tail, hs_handle** out);
+
+/* Free everything the handle owns.  Synchronises the device first.  NULL is a no-op. */
+void hs_destroy(hs_handle* h);
+
+/*
+ * One decode step for all B requests: resolve topk_idx (device, [B][K]) into
+ * out_slot (device, [B][K]) and fetch every missing row from the host pool
+ * into the device buffer, on `stream`.  1 <= K <= min(S, HS_MAX_TOPK).
+ * Asynchronous; graph-capturable.  Calls on one handle must be ordered (one
+ * stream, or streams joined by events): each step reads the state the
+ * previous step wrote.
+ */
+int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+               hs_stream_t stream);
+
+/*
+ * The same step from host memory: copies topk_idx (host, [B][K]) to the
+ * device, resolves, copies out_slot (host, [B][K]) back and synchronises the
+ * stream before returning.  Pinned host buffers give the fastest copies.
+ * Not graph-capturable (it synchronises).
+ */
+int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                    hs_stream_t stream);
+
+/*
+ * Read the counters and, if last_miss is not NULL, the last step's miss count
+ * of every request (host, [B]).  Synchronises the device first.
+ */
+int hs_stats(hs_handle* h, hs_stats_t* out, int32_t* last_miss);
+
+/* Host pointer of the pinned, device-mapped host pool [B][H][R]; its size in bytes. */
+uint8_t* hs_host_pool(hs_handle* h);
+size_t hs_host_pool_bytes(hs_handle* h);
+
+/* Device pointer of the buffer [B][S+T][R] that out_slot indexes; its size in bytes. */
+uint8_t* hs_device_buffer(hs_handle* h);
+size_t hs_device_buffer_bytes(hs_handle* h);
+
+/*
+ * Set the current length of every request (host, [B]; each in [0, C]).
+ * Setup only: synchronises the device first.
+ */
+int hs_set_lengths(hs_handle* h, const int32_t* len_host);
+
+/*
+ * Mixed residency, growing context: for every request b write row b of
+ * rows_dev (device, [B][R]) as token len[b] into tail slot S + (len[b] mod T)
+ * and advance len[b].  A request whose next token is outside the tail
+ * ([C - T, C)) is left unchanged and HS_E_APPEND is latched.  Asynchronous;
+ * graph-capturable.  Requires T > 0.
+ */
+int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream);
+
+/*
+ * Setup only: write tokens [first_token, first_token + n) of request b from
+ * rows_host (host, [n][R]) into their tail slots S + (t mod T).  All tokens
+ * must lie in [C - T, C).  Synchronous.
+ */
+int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t* rows_host);
+
+/*
+ * Copy the state to host memory (any pointer may be NULL to skip it):
+ * tok_slot [B][C], slot_tok [B][S], stamp [B][S], step (one int32).
+ * Synchronises the device first.
+ */
+int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp,
+                    int32_t* step);
+
+/* Copy request b's buffer rows [S+T][R] to host memory.  Synchronous. */
+int hs_export_buffer(hs_handle* h, int b, uint8_t* dst_host);
+
+/* Back to the start state: empty tables, stamps 0, step 0, counters and error bits 0,
+ * lengths = C.  The host pool and buffer bytes are kept.  Synchronous. */
+int hs_reset(hs_handle* h);
+
+/*
+ * Measurement helper: stream `bytes` (a multiple of 16) from pinned host
+ * memory `src_host` (allocated with cudaHostAlloc(..., cudaHostAllocMapped)
+ * or returned by hs_host_pool) into device memory `dst_dev` with 128-bit
+ * zero-copy loads -- the access pattern of the row fetch, but sequential.
+ * `blocks` = 0 picks the default grid.  Asynchronous.
+ */
+int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
+                hs_stream_t stream);
+
+/*
+ * Measurement aid: when `before_copy` and `after_copy` (cudaEvent_t) are not
+ * NULL, every later hs_resolve on this handle records them on its stream
+ * around the row-copy kernel, so the copy's own duration can be read with
+ * cudaEventElapsedTime.  The copy then no longer overlaps the tail of the
+ * resolve kernel.  Pass NULL, NULL to switch it off.
+ */
+int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy);
+
+/* Static text for a return code. */
+const char* hs_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H */

@@ -112,9 +112,11 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
 
     ``append_rows`` [steps][R], when given, is appended before each step's
     resolve (a growing context with a resident tail).  Returns
-    (state, out [steps][K], counts [steps][3], err_bits [steps]).
+    (state, out [steps][K], counts [steps][3], resolve error bits [steps]);
+    ``state.append_errs`` holds the OR of the appends' error bits.
     """
     st = RequestState(C, S, T, R, length)
+    st.append_errs = 0
     if tail_init is not None:
         tail_init(st)
     steps = topk_rows.shape[0]
@@ -122,13 +124,12 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
     counts = np.empty((steps, 3), dtype=np.int64)
     errs = np.empty(steps, dtype=np.int32)
     for s in range(steps):
-        e = 0
         if append_rows is not None:
-            e |= st.append(append_rows[s])
-        o, c, e2 = st.resolve(host, topk_rows[s], step0 + s + 1)
+            st.append_errs |= st.append(append_rows[s])
+        o, c, e = st.resolve(host, topk_rows[s], step0 + s + 1)
         outs[s] = o
         counts[s] = c
-        errs[s] = e | e2
+        errs[s] = e
     return st, outs, counts, errs
 
 

@@ -1,0 +1,126 @@
+"""Run a workload on the GPU through the C ABI and compare it, request by
+request, with the CPU oracle.  Used by the GPU parity tests and the smoke check.
+
+Every comparison is exact (integer and byte work): per-step out_slot, per-step
+miss counts, the final token->slot / slot->token tables and stamps, the step
+counter, the cumulative counters, and the bytes of every occupied buffer slot
+and every written tail slot.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from hierarchical_kv_cache_hs_gb300 import hs
+from hierarchical_kv_cache_hs_gb300 import tracegen as tg
+from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+
+
+class GpuResult:
+    pass
+
+
+def gpu_run(wl, steps=None, trace=None, graph=False, setup=None):
+    """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one."""
+    w = GpuWorkload(wl, steps=steps, record=True)
+    if setup is not None:
+        setup(w)
+    if trace is not None:
+        w.topk = torch.from_numpy(np.ascontiguousarray(trace, dtype=np.int32)).cuda()
+    steps = w.steps
+    res = GpuResult()
+    res.misses = np.zeros((wl.layers, steps, wl.B), dtype=np.int32)
+    stream = torch.cuda.Stream()
+    if graph:
+        # Warm the kernels up outside the capture, then restart from the empty state.
+        with torch.cuda.stream(stream):
+            w.launch_step(0, stream)
+        stream.synchronize()
+        w.reset()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(steps):
+                w.launch_step(s, torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        res.misses = None  # per-step counts are not observable inside one graph
+    else:
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                w.launch_step(s, stream)
+                for layer, h in enumerate(w.handles):
+                    hs.hs_stats(h.h, res.misses[layer, s])
+    torch.cuda.synchronize()
+    res.out = w.out.cpu().numpy()
+    res.trace = w.topk.cpu().numpy()
+    res.stats = [h.stats() for h in w.handles]
+    res.state = [h.export_state() for h in w.handles]
+    res.workload = w
+    return res
+
+
+def oracle_request(wl, layer, b, trace_lb, steps):
+    host = tg.rows(wl, layer, b, 0, wl.cold)
+    append_rows = tg.rows(wl, layer, b, wl.len0, steps) if wl.grow else None
+    tail_init = None
+    if wl.T > 0 and not wl.grow:
+        tail = tg.rows(wl, layer, b, wl.cold, wl.T)
+
+        def tail_init(st, tail=tail):
+            for i in range(wl.T):
+                t = wl.cold + i
+                st.buf[wl.S + t % wl.T] = tail[i]
+    length = wl.len0 if wl.grow else wl.C
+    return oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace_lb, length=length,
+                              append_rows=append_rows, tail_init=tail_init)
+
+
+def compare(wl, res, requests=None, layers=None):
+    """Compare the GPU run with the oracle on the given requests; returns oracle totals."""
+    steps = res.out.shape[1]
+    layers = range(wl.layers) if layers is None else layers
+    requests = range(wl.B) if requests is None else requests
+    jobs = [(l, b) for l in layers for b in requests]
+    R = wl.row_bytes
+
+    def one(job):
+        layer, b = job
+        st, outs, counts, errs = oracle_request(wl, layer, b, res.trace[layer, :, b], steps)
+        tok, slot_tok, stamp, step = res.state[layer]
+        ctx = "layer %d request %d" % (layer, b)
+        np.testing.assert_array_equal(res.out[layer, :, b], outs, err_msg=ctx + " out_slot")
+        if res.misses is not None:
+            np.testing.assert_array_equal(res.misses[layer, :, b], counts[:, 1], err_msg=ctx + " misses")
+        np.testing.assert_array_equal(tok[b], st.tok_slot, err_msg=ctx + " tok_slot")
+        np.testing.assert_array_equal(slot_tok[b], st.slot_tok, err_msg=ctx + " slot_tok")
+        np.testing.assert_array_equal(stamp[b], st.stamp, err_msg=ctx + " stamp")
+        assert step == steps
+        buf = res.workload.handles[layer].export_buffer(b)
+        occ = np.nonzero(st.slot_tok >= 0)[0]
+        np.testing.assert_array_equal(buf[occ], st.buf[occ], err_msg=ctx + " buffer bytes")
+        if wl.T > 0:
+            last = int(st.len[0])
+            toks = np.arange(wl.cold, last)
+            tslots = wl.S + toks % wl.T
+            np.testing.assert_array_equal(buf[tslots], st.buf[tslots], err_msg=ctx + " tail bytes")
+        return counts.sum(axis=0), int(np.bitwise_or.reduce(errs)) if len(errs) else 0
+
+    results = oracle.parallel_map(one, jobs)
+    tot = np.zeros(3, dtype=np.int64)
+    err = 0
+    for c, e in results:
+        tot += c
+        err |= e
+    return tot, err
+
+
+def check_counters(wl, res, tot, err):
+    """Cumulative counters must equal the oracle's sums (all requests compared)."""
+    hits = sum(s["hits"] for s in res.stats)
+    misses = sum(s["misses"] for s in res.stats)
+    inplace = sum(s["inplace"] for s in res.stats)
+    assert (hits, misses, inplace) == tuple(int(x) for x in tot)
+    assert sum(s["bytes_copied"] for s in res.stats) == misses * wl.row_bytes
+    for s in res.stats:
+        assert s["err_bits"] == err
