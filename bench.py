@@ -194,7 +194,11 @@ def run_ours(args, rank, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.SUM)
         return float(t.item())
 
-    peaks = measure_h2d_peak(torch, hs)
+    if args.no_peaks:
+        peaks = {"copy_engine_gbs": None, "zero_copy_kernel_gbs": None, "peak_gbs": float("nan"),
+                 "zero_copy_checked": None, "bytes": 0}
+    else:
+        peaks = measure_h2d_peak(torch, hs)
     hbm_gbs, hbm_src = measure_hbm_peak(torch)
 
     def measure(wl, want_profile=True, want_e2e=True):
@@ -293,7 +297,7 @@ def run_ours(args, rank, world, dist):
 
     sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
-    main = measure(wl)
+    main = measure(wl, want_e2e=not args.no_e2e)
     clocks = sampler.stop()
 
     sweep = {}
@@ -327,7 +331,7 @@ def run_ours(args, rank, world, dist):
         t_roof += max(m * wl.row_bytes / (h2d_peak * 1e9), table / (hbm_gbs * 1e9))
     step_frac = t_roof / (main["dev_ms"] / 1e3)
 
-    e2e_value = all_units / max_over_ranks(main["e2e_s"])
+    e2e_value = all_units / max_over_ranks(main["e2e_s"]) if "e2e_s" in main else None
     line = {
         "metric": METRIC,
         "value": value,
@@ -461,6 +465,9 @@ def main():
     ap.add_argument("--workload", default="b64_c64k_s4096")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-peaks", action="store_true",
+                    help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
