@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libhs.so")
 
-SOURCES = ["hs_api.cpp", "hs_resolve.cu", "hs_copy.cu"]
+SOURCES = ["hs_api.cpp", "hs_resolve.cu", "hs_copy.cu", "hs_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "hs_internal.h"), os.path.join(INCLUDE, "hs.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -79,6 +79,7 @@ def _load():
         "hs_reset": ([P], I),
         "hs_h2d_read": ([P, P, Z, I, P], I),
         "hs_profile_events": ([P, P, P], I),
+        "hs_resolve_noalloc": ([I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], I),
         "hs_error_string": ([I], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -213,6 +214,25 @@ def hs_reset(h: int) -> None:
 def hs_h2d_read(src_host, dst_dev, nbytes: int, blocks: int = 0, stream=None) -> None:
     _check(lib.hs_h2d_read(_ptr(src_host), _ptr(dst_dev), int(nbytes), int(blocks),
                            _stream(stream)), "hs_h2d_read")
+
+
+HS_NOALLOC_MAX_ENTRIES = 524288
+
+
+def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resident_tail,
+                       topk_idx, K, out_slot, tok_slot, slot_tok, stamp, lengths, host_pool,
+                       device_buffer, control, stream=None) -> None:
+    """The swap-in step on caller-owned state; the library allocates nothing.
+
+    For callers that cannot let a library allocate device memory (an engine
+    that reserved HBM for its own pool, a loop where an allocation would stall
+    the device).  ``control`` is a zeroed 32-byte device block (hs_control_t).
+    """
+    _check(lib.hs_resolve_noalloc(int(batch), int(ctx_len), int(row_bytes), int(buffer_slots),
+                                  int(host_rows), int(resident_tail), _ptr(topk_idx), int(K),
+                                  _ptr(out_slot), _ptr(tok_slot), _ptr(slot_tok), _ptr(stamp),
+                                  _ptr(lengths), _ptr(host_pool), _ptr(device_buffer),
+                                  _ptr(control), _stream(stream)), "hs_resolve_noalloc")
 
 
 def hs_profile_events(h: int, before_copy=None, after_copy=None) -> None:

@@ -203,6 +203,49 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
  */
 int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy);
 
+/*
+ * ---- Allocation-free variant -------------------------------------------
+ * (The pages have no counterpart: this entry point exists for callers of the
+ * library, not because the method needs it.)
+ *
+ * For callers that must not have a library allocate device memory -- an
+ * engine that has reserved nearly all HBM for its own KV pool, or a decode
+ * loop in which an allocation would synchronise the device.  The caller owns
+ * all state and passes it in; the step is the same as hs_resolve's.
+ *
+ *   tok_slot [B][C], slot_tok [B][S] (start at -1), stamp [B][S] (start at 0),
+ *   lengths [B], device_buffer [B][S+T][R]: device memory.
+ *   host_pool [B][host_rows][R]: pinned host memory mapped into the device
+ *   address space (cudaHostAlloc with cudaHostAllocMapped), host pointer.
+ *   control: device memory, one hs_control_t, zeroed by the caller before
+ *   the first step; the step counter and counters advance in it.
+ *
+ * The per-step miss lists live in a fixed device array inside the library
+ * (HS_NOALLOC_SCRATCH_BYTES, held on every device that loads the library
+ * until the process exits), so B * K may not exceed HS_NOALLOC_MAX_ENTRIES
+ * (HS_ERR_LIMIT otherwise).  The first call on a device looks up that
+ * array's address and sets kernel attributes; make that first call before
+ * any stream capture.  All calls on a device share the array: calls whose
+ * work overlaps on the GPU race, so order them on one stream.  Returns
+ * HS_OK or an HS_ERR_* code, synchronously, like hs_resolve.
+ */
+#define HS_NOALLOC_MAX_ENTRIES    524288   /* B * K */
+#define HS_NOALLOC_SCRATCH_BYTES  (2 * 4 * HS_NOALLOC_MAX_ENTRIES + 4 * HS_MAX_BATCH)
+
+typedef struct {
+    int32_t step;       /* resolves done; this call's step is step + 1 */
+    int32_t err_bits;   /* HS_E_* bits, OR-ed in */
+    uint64_t hits;      /* cumulative counters, added to */
+    uint64_t misses;
+    uint64_t inplace;
+} hs_control_t;
+
+int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_rows,
+                       int resident_tail, const int32_t* topk_idx, int K, int32_t* out_slot,
+                       int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp,
+                       const int32_t* lengths, const uint8_t* host_pool, uint8_t* device_buffer,
+                       hs_control_t* control, hs_stream_t stream);
+
 /* Static text for a return code. */
 const char* hs_error_string(int code);
 
