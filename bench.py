@@ -163,6 +163,41 @@ def measure_hbm_peak(torch):
     return 2 * n / best / 1e6, "device copy measured in this run (read + write bytes)"
 
 
+# ---------------------------------------------------------------- ranks
+def shard_requests(rank: int, batch: int):
+    """Request ids of one rank: each rank owns its own block of B requests.
+
+    The path partitions by request (every request owns its tables, stamps,
+    buffer and host rows), so ranks share nothing on the data path."""
+    return list(range(rank * batch, (rank + 1) * batch))
+
+
+class RankOps:
+    """Timing-only collectives over the ranks (none on the data path)."""
+
+    def __init__(self, dist, device):
+        self.dist = dist
+        self.device = device
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def _reduce(self, x, op):
+        if self.dist is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    def max(self, x):
+        return self._reduce(x, None if self.dist is None else self.dist.ReduceOp.MAX)
+
+    def sum(self, x):
+        return self._reduce(x, None if self.dist is None else self.dist.ReduceOp.SUM)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, dist):
     import torch
@@ -171,28 +206,15 @@ def run_ours(args, rank, world, dist):
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
 
     wl = tg.WORKLOADS[args.workload]
+    mode = {"auto": hs.HS_COPY_AUTO, "fused": hs.HS_COPY_FUSED, "split": hs.HS_COPY_SPLIT}[args.copy_mode]
+    fused = mode == hs.HS_COPY_FUSED or (mode == hs.HS_COPY_AUTO and wl.B >= hs.HS_FUSED_MIN_BATCH)
     total_steps = PRIME_STEPS + args.warmup + args.steps
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+    ops = RankOps(dist, dev)
+    barrier, max_over_ranks, sum_over_ranks = ops.barrier, ops.max, ops.sum
 
     if args.no_peaks:
         peaks = {"copy_engine_gbs": None, "zero_copy_kernel_gbs": None, "peak_gbs": float("nan"),
@@ -203,7 +225,7 @@ def run_ours(args, rank, world, dist):
 
     def measure(wl, want_profile=True, want_e2e=True):
         w = GpuWorkload(wl, steps=total_steps, record=False, host_trace=want_e2e,
-                        request_offset=rank * wl.B)
+                        request_offset=shard_requests(rank, wl.B)[0], copy_mode=mode)
         stream = torch.cuda.Stream(device=dev)
         res = {}
         try:
@@ -350,6 +372,7 @@ def run_ours(args, rank, world, dist):
             "prime_steps_untimed": PRIME_STEPS,
             "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
             "parallelism": "requests sharded over ranks, no collective on the data path",
+            "launch_mode": "fused" if fused else "split",
         },
         "miss_row_gbs": miss_gbs,
         "h2d_peak": peaks,
@@ -358,13 +381,17 @@ def run_ours(args, rank, world, dist):
                           "frac": step_frac,
                           "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
                           "table_bytes_per_resolve": "16K + 4S + 16m"},
-        "roofline": {"bound": "h2d", "kernel": "hs_copy_kernel", "achieved": copy_gbs,
+        "roofline": {"bound": "h2d",
+                     "kernel": "hs_resolve_kernel<fused> (resolve + row fetch)" if fused else "hs_copy_kernel",
+                     "achieved": copy_gbs,
                      "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
                      "traffic": None,
                      "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
                                     "1 GiB zero-copy 128-bit read kernel)"},
-        "kernel_ms_per_step": {"copy": sum(main["copy_ms"]) / args.steps,
-                               "resolve": sum(main["resolve_ms"]) / args.steps},
+        "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if fused else
+                               {"copy": sum(main["copy_ms"]) / args.steps,
+                                "resolve": sum(main["resolve_ms"]) / args.steps}),
+        "launch_mode": "fused" if fused else "split",
         "misses_per_step_mean": statistics.mean(main["misses_per_step"]),
         "misses_per_step": main["misses_per_step"],
         "e2e": {"value": e2e_value, "unit": "resolves/s",
@@ -468,6 +495,8 @@ def main():
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass")
+    ap.add_argument("--copy-mode", choices=["auto", "fused", "split"], default="auto",
+                    help="launch mode of the step (identical results; see hs_set_copy_mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -24,9 +24,11 @@ struct hs_handle {
     int32_t* d_miss_slot;  // [B][S] scratch: their victim slots
     int32_t* d_miss_cnt;   // [B]
     HsDevState* d_st;
+    unsigned* d_done;      // CTAs finished in the current fused launch
     int32_t* d_stage_in;   // [B][min(S, HS_MAX_TOPK)] for hs_resolve_host
     int32_t* d_stage_out;
     cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
+    int copy_mode;         // HS_COPY_*
     int copy_grid;
     int copy_unroll;
     int copy_rows_per_group;
@@ -71,6 +73,7 @@ void free_all(hs_handle* h)
     cudaFree(h->d_miss_slot);
     cudaFree(h->d_miss_cnt);
     cudaFree(h->d_st);
+    cudaFree(h->d_done);
     cudaFree(h->d_stage_in);
     cudaFree(h->d_stage_out);
     if (h->h_pool) cudaFreeHost(h->h_pool);
@@ -84,6 +87,7 @@ int fill_start_state(hs_handle* h)
     if (cudaMemset(h->d_stamp, 0, B * h->S * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaMemset(h->d_miss_cnt, 0, B * sizeof(int32_t)) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaMemset(h->d_st, 0, sizeof(HsDevState)) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemset(h->d_done, 0, sizeof(unsigned)) != cudaSuccess) return HS_ERR_CUDA;
     std::vector<int32_t> len(B, h->C);
     if (cudaMemcpy(h->d_len, len.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess)
         return HS_ERR_CUDA;
@@ -161,6 +165,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
               dalloc(&h->d_miss_slot, B * buffer_slots) == cudaSuccess &&
               dalloc(&h->d_miss_cnt, B) == cudaSuccess &&
               dalloc(&h->d_st, 1) == cudaSuccess &&
+              dalloc(&h->d_done, 1) == cudaSuccess &&
               dalloc(&h->d_stage_in, B * kmax) == cudaSuccess &&
               dalloc(&h->d_stage_out, B * kmax) == cudaSuccess;
     if (ok) {
@@ -190,6 +195,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_unroll = hs_copy_unroll_for(row_bytes);
     h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
+    h->copy_mode = HS_COPY_AUTO;
     const int rc = fill_start_state(h);
     if (rc != HS_OK) {
         free_all(h);
@@ -237,6 +243,24 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
     ra.cold = h->cold;
     ra.list_stride = h->S;
     ra.hash_bits = hs_hash_bits(K);
+    ra.pool = h->d_pool;
+    ra.buf = h->d_buf;
+    ra.H = h->H;
+    ra.R = h->R;
+    ra.rows_per_group = h->copy_rows_per_group;
+    ra.done = h->d_done;
+
+    const bool prof = h->prof_before && h->prof_after;
+    const bool fused = h->copy_mode == HS_COPY_FUSED ||
+                       (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
+    if (fused) {
+        // One launch: each request's CTA fetches its own rows.  The profiling
+        // events then bracket the whole step.
+        if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
+        if (hs_launch_swapin(ra, h->B, h->copy_unroll, s) != cudaSuccess) return HS_ERR_CUDA;
+        if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
+        return HS_OK;
+    }
     if (hs_launch_resolve(ra, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
 
     CopyArgs ca;
@@ -254,10 +278,24 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
     ca.H = h->H;
     ca.rows_per_group = h->copy_rows_per_group;
     ca.advance_step = 1;
-    const bool prof = h->prof_before && h->prof_after;
     if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
     if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
     if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_resolve_launches(hs_handle* h)
+{
+    if (!valid(h)) return HS_ERR_ARG;
+    const bool fused = h->copy_mode == HS_COPY_FUSED ||
+                       (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
+    return fused ? 1 : 2;
+}
+
+int hs_set_copy_mode(hs_handle* h, int mode)
+{
+    if (!valid(h) || mode < HS_COPY_AUTO || mode > HS_COPY_SPLIT) return HS_ERR_ARG;
+    h->copy_mode = mode;
     return HS_OK;
 }
 
@@ -381,6 +419,49 @@ int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t*
             return HS_ERR_CUDA;
         *step = st.step;
     }
+    return HS_OK;
+}
+
+int hs_import_state(hs_handle* h, const int32_t* tok_slot, const int32_t* slot_tok,
+                    const int32_t* stamp, int32_t step)
+{
+    if (!valid(h) || !tok_slot || !slot_tok || !stamp || step < 0) return HS_ERR_ARG;
+    const size_t C = (size_t)h->C, S = (size_t)h->S;
+    for (int b = 0; b < h->B; ++b) {
+        const int32_t* ts = tok_slot + (size_t)b * C;
+        const int32_t* st = slot_tok + (size_t)b * S;
+        const int32_t* sp = stamp + (size_t)b * S;
+        size_t occupied = 0;
+        for (size_t v = 0; v < S; ++v) {
+            const int32_t t = st[v];
+            if (sp[v] < 0 || sp[v] > step) return HS_ERR_ARG;
+            if (t == -1) continue;
+            if (t < 0 || t >= h->cold || ts[t] != (int32_t)v) return HS_ERR_ARG;
+            ++occupied;
+        }
+        size_t mapped = 0;
+        for (size_t t = 0; t < C; ++t) {
+            const int32_t v = ts[t];
+            if (v == -1) continue;
+            if (v < 0 || (size_t)v >= S || (int)t >= h->cold || st[v] != (int32_t)t) return HS_ERR_ARG;
+            ++mapped;
+        }
+        if (mapped != occupied) return HS_ERR_ARG;
+    }
+    DeviceGuard g(h->device);
+    if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
+    const size_t B = (size_t)h->B;
+    if (cudaMemcpy(h->d_tok_slot, tok_slot, B * C * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(h->d_slot_tok, slot_tok, B * S * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(h->d_stamp, stamp, B * S * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess)
+        return HS_ERR_CUDA;
+    HsDevState st = {};
+    st.step = step;
+    if (cudaMemcpy(h->d_st, &st, sizeof(st), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(h->d_done, 0, sizeof(unsigned)) != cudaSuccess)
+        return HS_ERR_CUDA;
     return HS_OK;
 }
 

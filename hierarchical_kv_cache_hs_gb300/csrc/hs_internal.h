@@ -32,6 +32,13 @@ struct ResolveArgs {
     int K, C, S, T, cold;
     int list_stride;
     int hash_bits;         // dedup hash capacity = 1 << hash_bits >= 2K
+    // Fused variant only: the row fetch and the step advance.
+    const uint8_t* pool;   // device-usable address of the mapped pinned pool [B][H][R]
+    uint8_t* buf;          // [B][S+T][R]
+    long long H;
+    int R;
+    int rows_per_group;
+    unsigned* done;        // CTAs finished this call (returns to 0 after each call)
 };
 
 struct CopyArgs {
@@ -55,14 +62,28 @@ struct AppendArgs {
     int S, T, R, C, cold;
 };
 
-// Resolve kernel launch geometry.
-constexpr int HS_RESOLVE_THREADS = 1024;
+// Launch geometry and shared-memory layout of the resolve kernel.
+constexpr int HS_RESOLVE_THREADS = 512;
 constexpr int HS_COPY_THREADS = 256;
+constexpr int HS_AGE_BINS = 1024;
+constexpr int HS_AGE_SUBHIST = 4;
+
+// Ints of the region shared by the dedup hash (2 << hash_bits) and the age
+// histograms (HS_AGE_SUBHIST * HS_AGE_BINS).
+__host__ __device__ inline int hs_resolve_region_a_ints(int hash_bits)
+{
+    const int hc2 = 2 << hash_bits;
+    const int hist = HS_AGE_SUBHIST * HS_AGE_BINS;
+    return hc2 > hist ? hc2 : hist;
+}
 
 size_t hs_resolve_smem_bytes(int K, int S);
 int hs_hash_bits(int K);
 cudaError_t hs_prepare_resolve();
+// Resolve only: writes the miss lists for hs_launch_copy.
 cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s);
+// Resolve + row fetch in one launch; advances the step counter itself.
+cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream_t s);
 
 // Copy kernel: `pdl` lets it launch while the resolve grid drains (it waits
 // on the resolve grid's completion before reading the miss lists).

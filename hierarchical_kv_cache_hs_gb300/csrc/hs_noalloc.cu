@@ -124,6 +124,12 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
     ra.cold = ctx_len - resident_tail;
     ra.list_stride = K;
     ra.hash_bits = hs_hash_bits(K);
+    ra.pool = nullptr;
+    ra.buf = nullptr;
+    ra.H = host_rows;
+    ra.R = row_bytes;
+    ra.rows_per_group = 1;
+    ra.done = nullptr;
     if (hs_launch_resolve(ra, batch, s) != cudaSuccess) return HS_ERR_CUDA;
 
     int sms = 1;

@@ -1,21 +1,36 @@
-// Resolve kernel of the HiSparse swap-in path: steps (1)-(3) of the swap-in
-// kernel of the HiSparse blog ("Efficient swap-in kernel"): miss
-// identification, LRU victim selection and the page-table update.  The host
-// row fetch of step (3) runs in the copy kernel that follows (hs_copy.cu).
+// Swap-in kernel of the HiSparse path: steps (1)-(3) of the HiSparse blog's
+// swap-in kernel ("Efficient swap-in kernel"): miss identification, LRU
+// victim selection, and the page-table update with the host -> device row
+// fetch.
 //
-// One CTA of 1024 threads per request.  Everything the request's step needs
+// One CTA of 512 threads per request.  Everything the request's step needs
 // stays in shared memory:
-//   - a 2K-entry open-addressing hash of the row's indices, which finds
-//     repeated indices (the first occurrence wins);
-//   - the request's S stamps (read once, written back once, coalesced);
+//   - the request's S stamps and S slot -> token entries, loaded once,
+//     together with the top-k row, at the start;
+//   - a 2K-entry open-addressing hash of the row's indices that finds
+//     repeated indices (the first occurrence wins), built while the
+//     page-table gathers are in flight;
 //   - the miss list in top-k row order (block scan of per-thread counts);
 //   - the victim list in ascending slot order.
-// Victims are the m smallest (stamp, slot) pairs.  A block-wide radix select
-// over the stamps (8-bit digits, most significant first, only the digits
-// that the current step counter can populate) finds the m-th smallest stamp
-// tau; every slot below tau is a victim, and so are the lowest-index slots
-// equal to tau until m are taken.  Slots hit in this step carry the current
-// step -- larger than every other stamp -- so they are never chosen.
+//
+// Victims are the m slots with the smallest (stamp, slot) pairs.  One
+// 1024-bin histogram of stamp ages (step - stamp, ages >= 1023 share the
+// oldest bin) locates the m-th oldest stamp tau: when it falls in an exact
+// bin, tau is that bin's stamp; when it falls in the shared oldest bin, a
+// radix select over the stamps of that bin (8-bit digits, most significant
+// first) finds it.  Every slot older than tau is a victim, and so are the
+// lowest-index slots with stamp tau until m are taken; one packed block scan
+// gives each victim its position in ascending slot order.  Slots hit in this
+// step carry the current step -- younger than every other slot -- so they
+// are never chosen.
+//
+// Two variants:
+//   FUSED   the CTA then updates the tables and copies its own missing rows
+//           from the mapped host pool into the buffer (zero-copy 128-bit
+//           loads, U in flight per lane); the last CTA to finish advances the
+//           step counter.  One launch per step.
+//   !FUSED  the CTA writes the miss / victim lists to global memory for the
+//           grid-wide copy kernel (hs_copy.cu), which advances the counter.
 #include <climits>
 
 #include "hs_internal.h"
@@ -24,11 +39,15 @@ namespace {
 
 constexpr int NT = HS_RESOLVE_THREADS;
 constexpr int NW = NT / 32;
-constexpr int EMAX = HS_MAX_TOPK / NT;  // top-k entries per thread
+constexpr int EMAX = HS_MAX_TOPK / NT;   // top-k entries per thread
+constexpr int NB = HS_AGE_BINS;          // age bins
+constexpr int NSUB = HS_AGE_SUBHIST;     // age sub-histograms (NW / NSUB warps share one)
+constexpr int BPT = NB / NT;             // bins per thread in the bin scan
 constexpr unsigned FULL = 0xffffffffu;
 
-static_assert(NW == 32, "block scans assume 32 warps");
+static_assert(NW <= 32, "one warp scans the warp totals");
 static_assert(EMAX * NT == HS_MAX_TOPK, "entries per thread");
+static_assert(BPT * NT == NB, "bins per thread");
 
 enum : int { C_NONE = 0, C_BAD = 1, C_TAIL = 2, C_HIT = 3, C_MISS = 4 };
 
@@ -36,7 +55,7 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 {
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        int n = __shfl_up_sync(FULL, v, d);
+        const int n = __shfl_up_sync(FULL, v, d);
         if (lane >= d) v += n;
     }
     return v;
@@ -49,7 +68,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_w, int* total)
     const int incl = warp_incl_scan(v, lane);
     if (lane == 31) s_w[warp] = incl;
     __syncthreads();
-    if (warp == 0) s_w[lane] = warp_incl_scan(s_w[lane], lane);
+    if (warp == 0) {
+        const int x = lane < NW ? s_w[lane] : 0;
+        const int y = warp_incl_scan(x, lane);
+        if (lane < NW) s_w[lane] = y;
+    }
     __syncthreads();
     const int off = warp ? s_w[warp - 1] : 0;
     *total = s_w[NW - 1];
@@ -57,106 +80,125 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_w, int* total)
     return off + incl - v;
 }
 
-__device__ __forceinline__ int hs_region_a_ints(int hash_bits)
+__device__ __forceinline__ uint4 ld_host_v4(const uint8_t* p)
 {
-    const int hc2 = 2 << hash_bits;
-    return hc2 > NW * 256 ? hc2 : NW * 256;
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
 }
 
+__device__ __forceinline__ void st_v4(uint8_t* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+template <bool FUSED, int U>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
 {
     extern __shared__ __align__(16) int smem[];
     __shared__ int s_w[32];
     __shared__ int s_cnt[3];  // hits, in-place, error bits
-    __shared__ int s_sel[2];  // selected digit, count below it
+    __shared__ int s_sel[3];  // selected bin / digit, count below it, flag
 
-    // The copy grid may be scheduled as soon as every resolve CTA is running;
-    // it waits for this grid's completion before reading anything.
-    asm volatile("griddepcontrol.launch_dependents;");
+    if (!FUSED) {
+        // The copy grid may be scheduled as soon as every resolve CTA is
+        // running; it waits for this grid's completion before reading.
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
 
+    const int K = a.K, S = a.S;
     const int hc = 1 << a.hash_bits;
-    int* s_hkey = smem;                                  // [hc]  (phase 1)
-    int* s_hj = smem + hc;                               // [hc]  (phase 1)
-    int* s_hist = smem;                                  // [NW][256] (phase 2, reuses the hash)
-    int* s_stamp = smem + hs_region_a_ints(a.hash_bits); // [S]
-    int* s_mtok = s_stamp + a.S;                         // [K]
-    int* s_mj = s_mtok + a.K;                            // [K]
-    int* s_vic = s_mj + a.K;                             // [K]
+    const int region_a = hs_resolve_region_a_ints(a.hash_bits);
+    int* s_hkey = smem;                       // [hc]   phase 1
+    int* s_hj = smem + hc;                    // [hc]   phase 1
+    int* s_hist = smem;                       // [NSUB][NB], phase 2 (reuses the hash)
+    int* s_stamp = smem + region_a;           // [S]
+    int* s_slot_tok = s_stamp + S;            // [S]
+    int* s_mtok = s_slot_tok + S;             // [K]
+    uint16_t* s_mj = reinterpret_cast<uint16_t*>(s_mtok + K);  // [K]
+    uint16_t* s_vic = s_mj + K;                                 // [K]
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = a.K, S = a.S;
     const int step = a.st->step + 1;
     const int len = a.len[b];
     const int32_t* g_topk = a.topk + (size_t)b * K;
     int32_t* g_out = a.out + (size_t)b * K;
     int32_t* g_stamp = a.stamp + (size_t)b * S;
-    const int32_t* g_tok_slot = a.tok_slot + (size_t)b * a.C;
+    int32_t* g_slot_tok = a.slot_tok + (size_t)b * S;
+    int32_t* g_tok_slot = a.tok_slot + (size_t)b * a.C;
 
-    for (int i = tid; i < hc; i += NT) {
-        s_hkey[i] = -1;
-        s_hj[i] = INT_MAX;
-    }
-    for (int i = tid; i < S; i += NT) s_stamp[i] = g_stamp[i];
-    if (tid < 3) s_cnt[tid] = 0;
-    __syncthreads();
-
-    // ---- (1) classify, drop repeats, gather the page table -------------
+    // ---- loads: top-k row (registers), stamps and slot -> token (shared) --
     // Thread tid owns the contiguous entries [tid*E, tid*E + E) so that a
     // block scan of per-thread miss counts yields row order.
     const int E = (K + NT - 1) / NT;
     const int j0 = tid * E;
-    int tk[EMAX], cl[EMAX], hs[EMAX], sl[EMAX];
+    int tk[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) tk[e] = (e < E && j0 + e < K) ? g_topk[j0 + e] : -1;
+    for (int i = tid; i < S; i += NT) {
+        s_stamp[i] = g_stamp[i];
+        s_slot_tok[i] = g_slot_tok[i];
+    }
+    for (int i = tid; i < hc; i += NT) {
+        s_hkey[i] = -1;
+        s_hj[i] = INT_MAX;
+    }
+    if (tid < 3) s_cnt[tid] = 0;
+    __syncthreads();
+
+    // ---- (1) classify, gather the page table, find repeats ----------------
+    int cl[EMAX], hs[EMAX], sl[EMAX];
     int err = 0;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
-        tk[e] = -1;
+        const int t = tk[e];
         cl[e] = C_NONE;
-        hs[e] = 0;
         sl[e] = -1;
-        const int j = j0 + e;
-        if (e < E && j < K) {
-            const int t = g_topk[j];
-            tk[e] = t;
-            if (t == -1) {
-                cl[e] = C_NONE;
-            } else if (t < -1 || t >= len || t >= a.C) {
+        hs[e] = 0;
+        if (e < E && j0 + e < K && t != -1) {
+            if (t < -1 || t >= len || t >= a.C) {
                 cl[e] = C_BAD;
                 err |= HS_E_RANGE;
             } else {
-                unsigned h = ((unsigned)t * 0x9E3779B1u) >> (32 - a.hash_bits);
-                for (;;) {
-                    const int k = atomicCAS(&s_hkey[h], -1, t);
-                    if (k == -1 || k == t) break;
-                    h = (h + 1) & (unsigned)(hc - 1);
-                }
-                atomicMin(&s_hj[h], j);
-                hs[e] = (int)h;
                 cl[e] = C_MISS;  // valid; refined below
+                if (t < a.cold) sl[e] = g_tok_slot[t];  // in flight during the hash
             }
         }
     }
-    __syncthreads();
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         if (cl[e] == C_MISS) {
-            if (s_hj[hs[e]] != j0 + e) {
-                cl[e] = C_BAD;
-                err |= HS_E_DUP;
-            } else if (tk[e] >= a.cold) {
-                cl[e] = C_TAIL;
-                sl[e] = S + tk[e] % a.T;
-            } else {
-                sl[e] = g_tok_slot[tk[e]];
+            const int t = tk[e];
+            unsigned h = ((unsigned)t * 0x9E3779B1u) >> (32 - a.hash_bits);
+            for (;;) {
+                const int k = atomicCAS(&s_hkey[h], -1, t);
+                if (k == -1 || k == t) break;
+                h = (h + 1) & (unsigned)(hc - 1);
             }
+            atomicMin(&s_hj[h], j0 + e);
+            hs[e] = (int)h;
         }
     }
+    __syncthreads();
     int nh = 0, ni = 0, nm = 0;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         const int j = j0 + e;
         if (cl[e] == C_MISS) {
-            if (sl[e] >= 0) {
+            if (s_hj[hs[e]] != j) {
+                cl[e] = C_BAD;
+                err |= HS_E_DUP;
+                g_out[j] = -1;
+            } else if (tk[e] >= a.cold) {
+                cl[e] = C_TAIL;
+                g_out[j] = S + tk[e] % a.T;
+                ++ni;
+            } else if (sl[e] >= 0) {
                 cl[e] = C_HIT;
                 s_stamp[sl[e]] = step;  // a hit refreshes its LRU entry
                 g_out[j] = sl[e];
@@ -164,9 +206,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
             } else {
                 ++nm;
             }
-        } else if (cl[e] == C_TAIL) {
-            g_out[j] = sl[e];
-            ++ni;
         } else if (e < E && j < K) {
             g_out[j] = -1;
         }
@@ -186,56 +225,105 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     for (int e = 0; e < EMAX; ++e) {
         if (cl[e] == C_MISS) {
             s_mtok[pos] = tk[e];
-            s_mj[pos] = j0 + e;
+            s_mj[pos] = (uint16_t)(j0 + e);
             ++pos;
         }
     }
 
     if (m > 0) {
-        // ---- (2) LRU victims: radix select of the m-th smallest stamp ----
-        const int nbits = 32 - __clz(step);
-        unsigned prefix = 0, pmask = 0;
-        int remaining = m;
+        // ---- (2) LRU victims ----------------------------------------------
+        // Age histogram: bin NB-1-min(age, NB-1), so older slots sit in lower
+        // bins and the shared bin 0 holds every age >= NB-1.
+        for (int i = tid; i < NSUB * NB; i += NT) s_hist[i] = 0;
+        __syncthreads();
         const int s_pad = (S + NT - 1) / NT * NT;
-        for (int d = (nbits - 1) >> 3; d >= 0; --d) {
-            const int shift = 8 * d;
-            for (int i = tid; i < NW * 256; i += NT) s_hist[i] = 0;
-            __syncthreads();
-            for (int i = tid; i < s_pad; i += NT) {
-                int dig = 256;
-                if (i < S) {
-                    const unsigned k = (unsigned)s_stamp[i];
-                    if ((k & pmask) == prefix) dig = (int)((k >> shift) & 255u);
-                }
-                const unsigned peers = __match_any_sync(FULL, dig);
-                if (dig < 256 && lane == __ffs(peers) - 1)
-                    atomicAdd(&s_hist[warp * 256 + dig], __popc(peers));
+        int* my_hist = s_hist + (warp % NSUB) * NB;
+        for (int i = tid; i < s_pad; i += NT) {
+            int bin = NB;
+            if (i < S) {
+                const int age = step - s_stamp[i];
+                bin = NB - 1 - (age < NB - 1 ? age : NB - 1);
             }
-            __syncthreads();
-            int c = 0, incl = 0;
-            if (tid < 256) {
-#pragma unroll 8
-                for (int w = 0; w < NW; ++w) c += s_hist[w * 256 + tid];
-                incl = warp_incl_scan(c, lane);
-                if (lane == 31) s_w[warp] = incl;
-            }
-            __syncthreads();
-            if (tid < 256) {
-                int off = 0;
-                for (int w = 0; w < warp; ++w) off += s_w[w];
-                const int excl = off + incl - c;
-                if (c > 0 && excl < remaining && remaining <= excl + c) {
-                    s_sel[0] = tid;
-                    s_sel[1] = excl;
-                }
-            }
-            __syncthreads();
-            prefix |= (unsigned)s_sel[0] << shift;
-            pmask |= 255u << shift;
-            remaining -= s_sel[1];
+            const unsigned peers = __match_any_sync(FULL, bin);
+            if (bin < NB && lane == __ffs(peers) - 1) atomicAdd(&my_hist[bin], __popc(peers));
         }
-        const int tau = (int)prefix;
-        const int need_eq = remaining;  // slots equal to tau taken, lowest index first
+        __syncthreads();
+        int c[BPT];
+        int csum = 0;
+#pragma unroll
+        for (int q = 0; q < BPT; ++q) {
+            const int bin = tid * BPT + q;
+            int x = 0;
+#pragma unroll
+            for (int h = 0; h < NSUB; ++h) x += s_hist[h * NB + bin];
+            c[q] = x;
+            csum += x;
+        }
+        int tot_bins;
+        int below = block_excl_scan(csum, s_w, &tot_bins);
+#pragma unroll
+        for (int q = 0; q < BPT; ++q) {
+            if (c[q] > 0 && below < m && m <= below + c[q]) {
+                s_sel[0] = tid * BPT + q;
+                s_sel[1] = below;
+            }
+            below += c[q];
+        }
+        __syncthreads();
+        const int bsel = s_sel[0];
+        int tau, need_eq;
+        if (bsel > 0) {
+            tau = step - (NB - 1 - bsel);  // one exact stamp per bin
+            need_eq = m - s_sel[1];
+        } else {
+            // The m-th oldest slot is among the ages >= NB-1: radix select
+            // over the stamps <= lim, most significant digit first.
+            const int lim = step - (NB - 1);
+            const int nbits = 32 - __clz(lim > 0 ? lim : 1);
+            unsigned prefix = 0, pmask = 0;
+            int remaining = m;
+            for (int d = (nbits - 1) >> 3; d >= 0; --d) {
+                const int shift = 8 * d;
+                for (int i = tid; i < NSUB * NB; i += NT) s_hist[i] = 0;
+                __syncthreads();
+                for (int i = tid; i < s_pad; i += NT) {
+                    int dig = 256;
+                    if (i < S) {
+                        const int k = s_stamp[i];
+                        if (k <= lim && ((unsigned)k & pmask) == prefix)
+                            dig = (int)(((unsigned)k >> shift) & 255u);
+                    }
+                    const unsigned peers = __match_any_sync(FULL, dig);
+                    if (dig < 256 && lane == __ffs(peers) - 1)
+                        atomicAdd(&my_hist[dig], __popc(peers));
+                }
+                __syncthreads();
+                int cd = 0, incl = 0;
+                if (tid < 256) {
+#pragma unroll
+                    for (int h = 0; h < NSUB; ++h) cd += s_hist[h * NB + tid];
+                    incl = warp_incl_scan(cd, lane);
+                    if (lane == 31) s_w[warp] = incl;
+                }
+                __syncthreads();
+                if (tid < 256) {
+                    int off = 0;
+                    for (int w = 0; w < warp; ++w) off += s_w[w];
+                    const int excl = off + incl - cd;
+                    if (cd > 0 && excl < remaining && remaining <= excl + cd) {
+                        s_sel[0] = tid;
+                        s_sel[1] = excl;
+                    }
+                }
+                __syncthreads();
+                prefix |= (unsigned)s_sel[0] << shift;
+                pmask |= 255u << shift;
+                remaining -= s_sel[1];
+                __syncthreads();
+            }
+            tau = (int)prefix;
+            need_eq = remaining;
+        }
 
         // Victims in ascending slot order: thread tid owns slots [tid*Q, tid*Q + Q).
         const int Q = (S + NT - 1) / NT;
@@ -260,32 +348,74 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 // stamp from writing past the list.
                 if (k < tau) {
                     const int p = lb + (eb < need_eq ? eb : need_eq);
-                    if (p < m) s_vic[p] = s;
+                    if (p < m) s_vic[p] = (uint16_t)s;
                     ++lb;
                 } else if (k == tau) {
-                    if (eb < need_eq && lb + eb < m) s_vic[lb + eb] = s;
+                    if (eb < need_eq && lb + eb < m) s_vic[lb + eb] = (uint16_t)s;
                     ++eb;
                 }
             }
         }
         __syncthreads();
 
-        // ---- (3) pair the i-th miss (row order) with the i-th victim ------
-        int32_t* g_slot_tok = a.slot_tok + (size_t)b * S;
-        int32_t* g_tok_slot_w = a.tok_slot + (size_t)b * a.C;
-        int32_t* g_mtok = a.miss_tok + (size_t)b * a.list_stride;
-        int32_t* g_mslot = a.miss_slot + (size_t)b * a.list_stride;
-        for (int i = tid; i < m; i += NT) {
-            const int t = s_mtok[i];
-            const int v = s_vic[i];
-            const int old = g_slot_tok[v];
-            if (old >= 0) g_tok_slot_w[old] = -1;  // the evicted token leaves the table
-            g_slot_tok[v] = t;
-            g_tok_slot_w[t] = v;
-            s_stamp[v] = step;
-            g_out[s_mj[i]] = v;
-            g_mtok[i] = t;
-            g_mslot[i] = v;
+        if (!FUSED) {
+            // ---- (3) pair the i-th miss (row order) with the i-th victim ----
+            int32_t* g_mtok = a.miss_tok + (size_t)b * a.list_stride;
+            int32_t* g_mslot = a.miss_slot + (size_t)b * a.list_stride;
+            for (int i = tid; i < m; i += NT) {
+                const int t = s_mtok[i];
+                const int v = s_vic[i];
+                const int old = s_slot_tok[v];
+                if (old >= 0) g_tok_slot[old] = -1;  // the evicted token leaves the table
+                g_slot_tok[v] = t;
+                g_tok_slot[t] = v;
+                s_stamp[v] = step;
+                g_out[s_mj[i]] = v;
+                g_mtok[i] = t;
+                g_mslot[i] = v;
+            }
+        } else {
+            // ---- (3) table update + host fetch, G rows per warp at a time ----
+            const int G = a.rows_per_group;
+            const int cpr = a.R >> 4;  // 16-byte chunks per row
+            const uint8_t* pool_b = a.pool + (size_t)b * (size_t)a.H * a.R;
+            uint8_t* buf_b = a.buf + (size_t)b * (size_t)(S + a.T) * a.R;
+            for (int r0 = warp * G; r0 < m; r0 += NW * G) {
+                long long src = 0, dst = 0;
+                const int i = r0 + lane;
+                if (lane < G && i < m) {
+                    const int t = s_mtok[i];
+                    const int v = s_vic[i];
+                    const int old = s_slot_tok[v];
+                    if (old >= 0) g_tok_slot[old] = -1;
+                    g_slot_tok[v] = t;
+                    g_tok_slot[t] = v;
+                    s_stamp[v] = step;
+                    g_out[s_mj[i]] = v;
+                    src = (long long)t * a.R;
+                    dst = (long long)v * a.R;
+                }
+                const int nrows = (m - r0) < G ? (m - r0) : G;
+                const int nch = nrows * cpr;
+                for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+                    uint4 v[U];
+                    long long d[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int cc = c0 + u * 32 + lane;
+                        const int rr = cc < nch ? cc / cpr : 0;
+                        const long long s = __shfl_sync(FULL, src, rr);
+                        const int off = (cc - rr * cpr) << 4;
+                        d[u] = __shfl_sync(FULL, dst, rr) + off;
+                        if (cc < nch) v[u] = ld_host_v4(pool_b + s + off);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int cc = c0 + u * 32 + lane;
+                        if (cc < nch) st_v4(buf_b + d[u], v[u]);
+                    }
+                }
+            }
         }
     }
     __syncthreads();
@@ -296,6 +426,16 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
         if (s_cnt[1]) atomicAdd(&a.st->inplace, (unsigned long long)s_cnt[1]);
         if (m) atomicAdd(&a.st->misses, (unsigned long long)m);
         if (s_cnt[2]) atomicOr(&a.st->err, s_cnt[2]);
+        if (FUSED) {
+            // Every CTA read the step counter before this point; the last one
+            // to arrive advances it for the next call and re-arms the count.
+            __threadfence();
+            const unsigned prev = atomicAdd(a.done, 1u);
+            if (prev == gridDim.x - 1) {
+                *a.done = 0u;
+                a.st->step = step;
+            }
+        }
     }
 }
 
@@ -310,17 +450,25 @@ int hs_hash_bits(int K)
 
 size_t hs_resolve_smem_bytes(int K, int S)
 {
-    const int hb = hs_hash_bits(K);
-    const int hc2 = 2 << hb;
-    const int region_a = hc2 > NW * 256 ? hc2 : NW * 256;
-    return sizeof(int) * ((size_t)region_a + (size_t)S + 3u * (size_t)K);
+    const int region_a = hs_resolve_region_a_ints(hs_hash_bits(K));
+    // ints: region A, stamps [S], slot -> token [S], miss tokens [K];
+    // uint16: miss row positions [K], victims [K]
+    return sizeof(int) * ((size_t)region_a + 2u * (size_t)S + (size_t)K) +
+           sizeof(uint16_t) * 2u * (size_t)K;
 }
 
 cudaError_t hs_prepare_resolve()
 {
-    const size_t most = hs_resolve_smem_bytes(HS_MAX_TOPK, HS_MAX_SLOTS);
-    return cudaFuncSetAttribute(hs_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)most);
+    const int most = (int)hs_resolve_smem_bytes(HS_MAX_TOPK, HS_MAX_SLOTS);
+    cudaError_t e = cudaFuncSetAttribute(hs_resolve_kernel<false, 9>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_resolve_kernel<true, 9>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_resolve_kernel<true, 8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    return e;
 }
 
 cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s)
@@ -330,5 +478,16 @@ cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s)
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = hs_resolve_smem_bytes(a.K, a.S);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, hs_resolve_kernel, a);
+    return cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false, 9>, a);
+}
+
+cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = hs_resolve_smem_bytes(a.K, a.S);
+    cfg.stream = s;
+    if (unroll == 9) return cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, 9>, a);
+    return cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, 8>, a);
 }

@@ -31,6 +31,11 @@ HS_E_RANGE = 1
 HS_E_DUP = 2
 HS_E_APPEND = 4
 
+HS_COPY_AUTO = 0
+HS_COPY_FUSED = 1
+HS_COPY_SPLIT = 2
+HS_FUSED_MIN_BATCH = 16
+
 HS_MAX_TOPK = 4096
 HS_MAX_SLOTS = 16384
 HS_MAX_BATCH = 4096
@@ -76,9 +81,12 @@ def _load():
         "hs_set_tail_rows": ([P, I, I, I, P], I),
         "hs_export_state": ([P, P, P, P, P], I),
         "hs_export_buffer": ([P, I, P], I),
+        "hs_import_state": ([P, P, P, P, I], I),
         "hs_reset": ([P], I),
         "hs_h2d_read": ([P, P, Z, I, P], I),
         "hs_profile_events": ([P, P, P], I),
+        "hs_set_copy_mode": ([P, I], I),
+        "hs_resolve_launches": ([P], I),
         "hs_resolve_noalloc": ([I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], I),
         "hs_error_string": ([I], ctypes.c_char_p),
     }
@@ -203,6 +211,22 @@ def hs_export_state(h: int, tok_slot=None, slot_tok=None, stamp=None) -> int:
     return int(step[0])
 
 
+def hs_import_state(h: int, tok_slot, slot_tok, stamp, step: int) -> None:
+    """Load a saved state (host arrays as hs_export_state writes them)."""
+    a = np.ascontiguousarray(tok_slot, dtype=np.int32)
+    b = np.ascontiguousarray(slot_tok, dtype=np.int32)
+    c = np.ascontiguousarray(stamp, dtype=np.int32)
+    _check(lib.hs_import_state(h, a.ctypes.data, b.ctypes.data, c.ctypes.data, int(step)),
+           "hs_import_state")
+
+
+def hs_import_state_rc(h: int, tok_slot, slot_tok, stamp, step: int) -> int:
+    a = np.ascontiguousarray(tok_slot, dtype=np.int32)
+    b = np.ascontiguousarray(slot_tok, dtype=np.int32)
+    c = np.ascontiguousarray(stamp, dtype=np.int32)
+    return lib.hs_import_state(h, a.ctypes.data, b.ctypes.data, c.ctypes.data, int(step))
+
+
 def hs_export_buffer(h: int, b: int, dst_host) -> None:
     _check(lib.hs_export_buffer(h, int(b), _ptr(dst_host)), "hs_export_buffer")
 
@@ -233,6 +257,17 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
                                   _ptr(out_slot), _ptr(tok_slot), _ptr(slot_tok), _ptr(stamp),
                                   _ptr(lengths), _ptr(host_pool), _ptr(device_buffer),
                                   _ptr(control), _stream(stream)), "hs_resolve_noalloc")
+
+
+def hs_set_copy_mode(h: int, mode: int) -> None:
+    _check(lib.hs_set_copy_mode(h, int(mode)), "hs_set_copy_mode")
+
+
+def hs_resolve_launches(h: int) -> int:
+    n = lib.hs_resolve_launches(h)
+    if n < 0:
+        raise HsError(n, "hs_resolve_launches")
+    return n
 
 
 def hs_profile_events(h: int, before_copy=None, after_copy=None) -> None:

@@ -27,7 +27,7 @@ class GpuWorkload:
 
     def __init__(self, wl: tg.Workload, steps: Optional[int] = None, record: bool = False,
                  device: str = "cuda", threads: Optional[int] = None, host_trace: bool = False,
-                 request_offset: int = 0):
+                 request_offset: int = 0, copy_mode: int = hs.HS_COPY_AUTO):
         self.wl = wl
         self.steps = wl.steps if steps is None else int(steps)
         self.device = torch.device(device)
@@ -39,6 +39,7 @@ class GpuWorkload:
         for layer in range(wl.layers):
             h = hs.Handle(B, wl.C, R, wl.S, wl.host_ratio, wl.T)
             self.handles.append(h)
+            hs.hs_set_copy_mode(h.h, copy_mode)
             # Cold rows of request b live at pool row t of request slot b.
             self._fill_pool(h, layer, reqs, threads)
             if wl.grow:
@@ -97,7 +98,7 @@ class GpuWorkload:
                 hs.hs_append(h.h, self.append_rows[layer, s], stream)
                 n += 1
             hs.hs_resolve(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), stream)
-            n += 2
+            n += hs.hs_resolve_launches(h.h)
         return n
 
     def host_step(self, s: int, out_host: torch.Tensor, stream=None) -> None:

@@ -177,6 +177,19 @@ int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t*
 int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp,
                     int32_t* step);
 
+/*
+ * Resume from a saved state: load tok_slot [B][C], slot_tok [B][S], stamp
+ * [B][S] (host arrays, the layout hs_export_state writes) and the step
+ * counter.  The state is checked on the host first and refused with
+ * HS_ERR_ARG unless it is one the path can reach: slot -> token entries in
+ * [-1, C - T), token -> slot entries in [-1, S) and -1 for tail tokens, the
+ * two maps inverse to each other, every stamp in [0, step], step >= 0.
+ * Buffer bytes are not part of the state (write them, or let misses refill
+ * them).  Counters and error bits are cleared.  Synchronous.
+ */
+int hs_import_state(hs_handle* h, const int32_t* tok_slot, const int32_t* slot_tok,
+                    const int32_t* stamp, int32_t step);
+
 /* Copy request b's buffer rows [S+T][R] to host memory.  Synchronous. */
 int hs_export_buffer(hs_handle* h, int b, uint8_t* dst_host);
 
@@ -195,11 +208,29 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
                 hs_stream_t stream);
 
 /*
+ * How the step is launched (both give identical results):
+ *   HS_COPY_FUSED  one kernel; each request's CTA resolves its row and then
+ *                  fetches its own missing rows from the host pool;
+ *   HS_COPY_SPLIT  a resolve kernel, then a grid-wide copy kernel over the
+ *                  misses of all requests (better when B is small);
+ *   HS_COPY_AUTO   fused when B >= HS_FUSED_MIN_BATCH, split otherwise (default).
+ */
+#define HS_COPY_AUTO   0
+#define HS_COPY_FUSED  1
+#define HS_COPY_SPLIT  2
+#define HS_FUSED_MIN_BATCH 16
+int hs_set_copy_mode(hs_handle* h, int mode);
+
+/* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG. */
+int hs_resolve_launches(hs_handle* h);
+
+/*
  * Measurement aid: when `before_copy` and `after_copy` (cudaEvent_t) are not
  * NULL, every later hs_resolve on this handle records them on its stream
- * around the row-copy kernel, so the copy's own duration can be read with
- * cudaEventElapsedTime.  The copy then no longer overlaps the tail of the
- * resolve kernel.  Pass NULL, NULL to switch it off.
+ * around the row-copy kernel (split mode) or around the single fused kernel
+ * (fused mode), so that kernel's duration can be read with
+ * cudaEventElapsedTime.  In split mode the copy then no longer overlaps the
+ * tail of the resolve kernel.  Pass NULL, NULL to switch it off.
  */
 int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy);
 

@@ -21,9 +21,9 @@ class GpuResult:
     pass
 
 
-def gpu_run(wl, steps=None, trace=None, graph=False, setup=None):
+def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO):
     """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one."""
-    w = GpuWorkload(wl, steps=steps, record=True)
+    w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
     if setup is not None:
         setup(w)
     if trace is not None:

@@ -27,9 +27,10 @@ def _built():
     oracle.build()
 
 
-def _run_and_compare(wl, steps=None, requests=None, graph=False, trace=None, expect_err=0):
+def _run_and_compare(wl, steps=None, requests=None, graph=False, trace=None, expect_err=0,
+                     copy_mode=0):
     from gpu_harness import check_counters, compare, gpu_run
-    res = gpu_run(wl, steps=steps, graph=graph, trace=trace)
+    res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode)
     try:
         tot, err = compare(wl, res, requests=requests)
         if requests is None:
@@ -147,13 +148,23 @@ def test_parity_invalid_and_padding():
     assert (res.out[0, 3] == -1).all() and (res.misses[0, 3] == 0).all()
 
 
-def test_graph_replay_matches_oracle():
+@pytest.mark.parametrize("mode", [1, 2], ids=["fused", "split"])
+def test_graph_replay_matches_oracle(mode):
     """The whole step sequence captured in one CUDA graph and replayed."""
     for name in ("tiny_b1_c8k", "b32_c32k_s4096"):
         wl = tg.WORKLOADS[name]
-        _run_and_compare(wl, steps=40, graph=True)
+        _run_and_compare(wl, steps=40, graph=True, copy_mode=mode)
     wl = tg.WORKLOADS["b256_c32k_grow_tail512"]
-    _run_and_compare(wl, steps=24, graph=True, requests=[0, 101, 255])
+    _run_and_compare(wl, steps=24, graph=True, requests=[0, 101, 255], copy_mode=mode)
+
+
+@pytest.mark.parametrize("name,mode", [("tiny_b1_c8k", 1), ("b32_c32k_s4096", 2),
+                                       ("b64_c64k_s4096", 2), ("ragged", 1),
+                                       ("max_sizes", 1), ("single_slot", 1)])
+def test_parity_other_launch_mode(name, mode):
+    """The launch mode that the default (fused from 16 requests up) does not pick."""
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    _run_and_compare(wl, copy_mode=mode)
 
 
 def test_resolve_host_matches_device_path():
