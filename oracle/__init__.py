@@ -27,6 +27,9 @@ E_RANGE = 1
 E_DUP = 2
 E_NOROOM = 8
 
+POLICY_LRU = 0
+POLICY_FIFO = 1
+
 
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` next to its source (gcc, no CUDA)."""
@@ -52,6 +55,10 @@ def load_library(path: str):
     lib.or_init.restype = None
     lib.or_resolve.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P]
     lib.or_resolve.restype = i32
+    if hasattr(lib, "or_resolve_policy"):
+        lib.or_resolve_policy.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
+                                          i32]
+        lib.or_resolve_policy.restype = i32
     lib.or_append.argtypes = [i32, i32, i32, i32, P, P, P]
     lib.or_append.restype = i32
     return lib
@@ -68,8 +75,10 @@ def _lib():
 class RequestState:
     """State of one request: tables, stamps, device-buffer model and length."""
 
-    def __init__(self, C: int, S: int, T: int, R: int, length: Optional[int] = None, lib=None):
+    def __init__(self, C: int, S: int, T: int, R: int, length: Optional[int] = None, lib=None,
+                 policy: int = POLICY_LRU):
         self.lib = lib if lib is not None else _lib()
+        self.policy = int(policy)
         self.C, self.S, self.T, self.R = int(C), int(S), int(T), int(R)
         self.tok_slot = np.empty(C, dtype=np.int32)
         self.slot_tok = np.empty(S, dtype=np.int32)
@@ -89,11 +98,15 @@ class RequestState:
         assert host.shape[0] >= self.C - self.T and host.shape[1] == self.R
         out = np.empty(topk.shape[0], dtype=np.int32)
         counts = np.zeros(3, dtype=np.int32)
-        err = self.lib.or_resolve(self.C, self.S, self.T, self.R, int(self.len[0]),
-                                self.tok_slot.ctypes.data, self.slot_tok.ctypes.data,
-                                self.stamp.ctypes.data, self.buf.ctypes.data, host.ctypes.data,
-                                topk.ctypes.data, int(topk.shape[0]), int(step),
-                                out.ctypes.data, counts.ctypes.data)
+        args = (self.C, self.S, self.T, self.R, int(self.len[0]),
+                self.tok_slot.ctypes.data, self.slot_tok.ctypes.data,
+                self.stamp.ctypes.data, self.buf.ctypes.data, host.ctypes.data,
+                topk.ctypes.data, int(topk.shape[0]), int(step),
+                out.ctypes.data, counts.ctypes.data)
+        if self.policy == POLICY_LRU:
+            err = self.lib.or_resolve(*args)
+        else:
+            err = self.lib.or_resolve_policy(*args, self.policy)
         return out, (int(counts[0]), int(counts[1]), int(counts[2])), int(err)
 
     def append(self, row: np.ndarray) -> int:
@@ -107,7 +120,7 @@ class RequestState:
 def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.ndarray,
                 length: Optional[int] = None, append_rows: Optional[np.ndarray] = None,
                 tail_init: Optional[Callable[[RequestState], None]] = None,
-                step0: int = 0):
+                step0: int = 0, policy: int = POLICY_LRU):
     """Replay ``topk_rows`` [steps][K] for one request from the empty state.
 
     ``append_rows`` [steps][R], when given, is appended before each step's
@@ -115,7 +128,7 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
     (state, out [steps][K], counts [steps][3], resolve error bits [steps]);
     ``state.append_errs`` holds the OR of the appends' error bits.
     """
-    st = RequestState(C, S, T, R, length)
+    st = RequestState(C, S, T, R, length, policy=policy)
     st.append_errs = 0
     if tail_init is not None:
         tail_init(st)

@@ -20,6 +20,12 @@
  *   memory into the LRU slot.  Its "No Residency" state is the start state
  *   here: an empty buffer, rows load only when the indexer selects them.
  *
+ * Eviction policy: the pages compare eviction strategies by their miss
+ * counts (HiSparse blog, "Efficient swap-in kernel": a larger buffer with
+ * LRU misses far less).  Besides LRU the oracle offers FIFO, the plainest
+ * alternative: a slot's stamp is the step it was filled, hits do not refresh
+ * it, and a slot hit in this step is still never evicted in that step.
+ *
  * Readings where the pages are silent (each is a plain choice):
  *   - one token per page: the table maps token -> slot;
  *   - a stamp is the step counter at last use (hit or fill); steps start
@@ -41,6 +47,9 @@
 #define OR_E_RANGE 1
 #define OR_E_DUP 2
 #define OR_E_NOROOM 8
+
+#define OR_POLICY_LRU 0
+#define OR_POLICY_FIFO 1
 
 typedef struct {
     int32_t stamp;
@@ -86,10 +95,10 @@ void or_init(int32_t C, int32_t S, int32_t* tok_slot, int32_t* slot_tok, int32_t
  *
  * Returns the error bits (OR_E_*).
  */
-int32_t or_resolve(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
-                   int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
-                   const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
-                   int32_t* out, int32_t* counts)
+int32_t or_resolve_policy(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                          int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                          const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                          int32_t* out, int32_t* counts, int32_t policy)
 {
     int32_t err = 0;
     int32_t hits = 0, nmiss = 0, inplace = 0;
@@ -126,9 +135,10 @@ int32_t or_resolve(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
         }
     }
 
-    /* A hit refreshes the slot's LRU entry. */
-    for (int32_t s = 0; s < S; ++s)
-        if (hit[s]) stamp[s] = step;
+    /* Under LRU a hit refreshes the slot's entry; under FIFO it does not. */
+    if (policy == OR_POLICY_LRU)
+        for (int32_t s = 0; s < S; ++s)
+            if (hit[s]) stamp[s] = step;
 
     /* Step 2: LRU victims among the slots not hit this step. */
     int32_t ncand = 0;
@@ -166,6 +176,16 @@ int32_t or_resolve(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
 
     free(seen); free(hit); free(miss_tok); free(miss_pos); free(cand); free(victims);
     return err;
+}
+
+/* The LRU step (the swap-in kernel's policy). */
+int32_t or_resolve(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                   int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                   const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                   int32_t* out, int32_t* counts)
+{
+    return or_resolve_policy(C, S, T, R, len, tok_slot, slot_tok, stamp, buf, host, topk, K,
+                             step, out, counts, OR_POLICY_LRU);
 }
 
 /*

@@ -14,6 +14,9 @@ mismatch:
   - victims are collected by walking from the head and skipping the slots hit
     in this step; they are then used in ascending slot order, paired with the
     misses in top-k row order.
+  - with ``fifo=True`` only refilled slots move to the most-recent end: hits
+    leave the order alone (first in, first out), but a slot hit in this step
+    is still skipped as a victim.
 
 Semantics: HiSparse blog, "Efficient swap-in kernel" (miss detection, LRU
 eviction, page-table update + host fetch); vLLM Hybrid HiSparse post, "Mixed
@@ -22,8 +25,9 @@ Residency" (tail read in place, hits refresh LRU, one row per miss).
 
 
 class LinkedLRU:
-    def __init__(self, S, T, C, length, host_row, tail_row=None):
+    def __init__(self, S, T, C, length, host_row, tail_row=None, fifo=False):
         self.S, self.T, self.C, self.len = S, T, C, length
+        self.fifo = fifo
         self.host_row = host_row          # token -> bytes
         self.content = [None] * S         # token held by each slot
         self.buf = [None] * (S + T)       # bytes per slot
@@ -106,7 +110,7 @@ class LinkedLRU:
             self.content[v] = t
             self.buf[v] = self.host_row(t)
             out[j] = v
-        touched = sorted(hit_set | set(victims))
+        touched = sorted(set(victims) if self.fifo else hit_set | set(victims))
         for s in touched:
             self._unlink(s)
         for s in touched:

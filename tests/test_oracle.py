@@ -60,12 +60,12 @@ def _parse_golden():
 
 def check_golden(oracle_mod, lib=None):
     cases = _parse_golden()
-    assert [c["name"] for c in cases] == ["A", "B"]
+    assert [c["name"] for c in cases] == ["A", "B", "F"]
     R = 16
     for case in cases:
         S, K, C, T, L = case["S"], case["K"], case["C"], case["T"], case["len"]
         host = _host_rows(C, T, R)
-        st = oracle_mod.RequestState(C, S, T, R, L, lib=lib)
+        st = oracle_mod.RequestState(C, S, T, R, L, lib=lib, policy=case.get("policy", 0))
         tail_rows = {}
         for t in case["tail"]:
             row = np.full(R, 200 + t, dtype=np.uint8)
@@ -148,14 +148,14 @@ def _random_row(rng, K, length, prev, p_bad):
     return row
 
 
-def check_against_simulator(oracle_mod, seeds, lib=None):
+def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False):
     R = 8
     for seed in seeds:
         rng = random.Random(seed)
         S, K, T, C, length, grow, steps = _random_case(rng)
         host = _host_rows(C, T, R)
-        st = oracle_mod.RequestState(C, S, T, R, length, lib=lib)
-        sim = LinkedLRU(S, T, C, length, host_row=lambda t: host[t].copy())
+        st = oracle_mod.RequestState(C, S, T, R, length, lib=lib, policy=1 if fifo else 0)
+        sim = LinkedLRU(S, T, C, length, host_row=lambda t: host[t].copy(), fifo=fifo)
         prev = None
         for s in range(1, steps + 1):
             if grow and rng.random() < 0.7:
@@ -183,6 +183,30 @@ def check_against_simulator(oracle_mod, seeds, lib=None):
 @pytest.mark.parametrize("seed_block", range(4))
 def test_oracle_matches_linked_list_lru(oracle_lib, seed_block):
     check_against_simulator(oracle_lib, range(seed_block * 600, (seed_block + 1) * 600))
+
+
+def test_oracle_fifo_matches_linked_list(oracle_lib):
+    """FIFO: only refills move a slot in the recency order."""
+    check_against_simulator(oracle_lib, range(5000, 5800), fifo=True)
+
+
+def test_lru_beats_fifo_on_reuse(oracle_lib, tracegen):
+    """The pages' comparison of eviction strategies: on a trace with reuse,
+    LRU misses less than FIFO at the same buffer size.  (With S = K every slot
+    is hit or refilled each step and the two policies coincide, so this uses
+    the 4096-slot buffer.)"""
+    wl = tracegen.WORKLOADS["b64_c64k_s4096"]
+    tr = tracegen.topk_trace(wl, steps=30, requests=[0, 1])
+    tot = {}
+    for policy in (0, 1):
+        m = 0
+        for i in range(2):
+            host = np.zeros((wl.cold, 16), np.uint8)
+            _, _, counts, _ = oracle_lib.run_request(wl.C, wl.S, wl.T, 16, host, tr[:, i],
+                                                     policy=policy)
+            m += counts[10:, 1].sum()
+        tot[policy] = m
+    assert tot[0] < tot[1]
 
 
 def _check_invariants(st, topk, out, step, host, S, T, C):
