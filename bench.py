@@ -223,7 +223,7 @@ def run_ours(args, rank, world, dist):
         peaks = measure_h2d_peak(torch, hs)
     hbm_gbs, hbm_src = measure_hbm_peak(torch)
 
-    def measure(wl, want_profile=True, want_e2e=True):
+    def measure(wl, want_profile=True, want_e2e=True, want_ce=False):
         w = GpuWorkload(wl, steps=total_steps, record=False, host_trace=want_e2e,
                         request_offset=shard_requests(rank, wl.B)[0], copy_mode=mode)
         stream = torch.cuda.Stream(device=dev)
@@ -297,6 +297,24 @@ def run_ours(args, rank, world, dist):
                         resolve_ms.append(rms)
                 res.update(misses_per_step=misses_per_step, copy_ms=copy_ms, resolve_ms=resolve_ms)
 
+            # --- copy-engine comparison variant (hs_resolve_ce) ------------
+            if want_ce:
+                w.reset()
+                n_ce = min(args.steps, 30)
+                with torch.cuda.stream(stream):
+                    for s in range(PRIME_STEPS + args.warmup):
+                        w.launch_step(s, stream)
+                    ce_s = 0.0
+                    for i in range(n_ce):
+                        s = PRIME_STEPS + args.warmup + i
+                        flush.fill_(i & 0xFF)
+                        stream.synchronize()
+                        t0 = time.perf_counter()
+                        w.launch_step(s, stream, copy_engine=True)
+                        stream.synchronize()
+                        ce_s += time.perf_counter() - t0
+                res.update(ce_s=ce_s, ce_steps=n_ce)
+
             # --- end to end through hs_resolve_host -----------------------
             if want_e2e:
                 w.reset()
@@ -319,7 +337,7 @@ def run_ours(args, rank, world, dist):
 
     sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
-    main = measure(wl, want_e2e=not args.no_e2e)
+    main = measure(wl, want_e2e=not args.no_e2e, want_ce=not args.no_ce)
     clocks = sampler.stop()
 
     sweep = {}
@@ -402,6 +420,16 @@ def run_ours(args, rank, world, dist):
         "clocks": clocks,
         "wall_s_timed_region": main["wall_s"],
     }
+    if "ce_s" in main:
+        ce_value = wl.B * wl.layers * main["ce_steps"] / main["ce_s"]
+        line["copy_engine_variant"] = {
+            "api": "hs_resolve_ce: miss tokens read back, host-thread gather into pinned staging, "
+                   "one cudaMemcpyAsync, device scatter (host wall time per step, synchronised)",
+            "resolves_per_s": ce_value,
+            "ms_per_step": main["ce_s"] * 1e3 / main["ce_steps"],
+            "steps": main["ce_steps"],
+            "faster": "zero-copy (hs_resolve)" if value > ce_value else "copy-engine (hs_resolve_ce)",
+        }
     if sweep:
         line["sweep"] = sweep
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -495,6 +523,7 @@ def main():
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass")
+    ap.add_argument("--no-ce", action="store_true", help="skip the copy-engine comparison variant")
     ap.add_argument("--copy-mode", choices=["auto", "fused", "split"], default="auto",
                     help="launch mode of the step (identical results; see hs_set_copy_mode)")
     args = ap.parse_args()

@@ -3,12 +3,90 @@
 // data on the resolve path; everything it enqueues is graph-capturable.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <condition_variable>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "hs_internal.h"
+
+namespace {
+
+// A fixed set of host threads that run `fn(task)` for every task of a batch
+// and return when all are done (used by the copy-engine variant's gather).
+class GatherPool {
+public:
+    explicit GatherPool(int n)
+    {
+        for (int i = 0; i < n; ++i) threads_.emplace_back([this] { loop(); });
+    }
+    ~GatherPool()
+    {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            stop_ = true;
+        }
+        cv_.notify_all();
+        for (auto& t : threads_) t.join();
+    }
+    void run(int ntasks, const std::function<void(int)>& fn)
+    {
+        if (ntasks <= 0) return;
+        std::unique_lock<std::mutex> g(mu_);
+        fn_ = &fn;
+        ntasks_ = ntasks;
+        next_.store(0);
+        left_ = ntasks;
+        ++gen_;
+        cv_.notify_all();
+        done_.wait(g, [this] { return left_ == 0; });
+        fn_ = nullptr;
+    }
+
+private:
+    void loop()
+    {
+        unsigned long long seen = 0;
+        for (;;) {
+            const std::function<void(int)>* fn;
+            int n;
+            {
+                std::unique_lock<std::mutex> g(mu_);
+                cv_.wait(g, [&] { return stop_ || gen_ != seen; });
+                if (stop_) return;
+                seen = gen_;
+                fn = fn_;
+                n = ntasks_;
+            }
+            int done = 0;
+            for (int t = next_.fetch_add(1); t < n; t = next_.fetch_add(1)) {
+                (*fn)(t);
+                ++done;
+            }
+            if (done) {
+                std::lock_guard<std::mutex> g(mu_);
+                left_ -= done;
+                if (left_ == 0) done_.notify_all();
+            }
+        }
+    }
+    std::vector<std::thread> threads_;
+    std::mutex mu_;
+    std::condition_variable cv_, done_;
+    const std::function<void(int)>* fn_ = nullptr;
+    int ntasks_ = 0;
+    int left_ = 0;
+    std::atomic<int> next_{0};
+    unsigned long long gen_ = 0;
+    bool stop_ = false;
+};
+
+}  // namespace
 
 struct hs_handle {
     int B, C, R, S, T, H, cold;
@@ -29,10 +107,17 @@ struct hs_handle {
     int32_t* d_stage_out;
     cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
     int copy_mode;         // HS_COPY_*
+    int policy;            // HS_POLICY_*
     int copy_grid;
     int copy_unroll;
     int copy_rows_per_group;
     size_t pool_bytes, buf_bytes;
+    // Copy-engine variant (allocated on its first call).
+    uint8_t* ce_h_stage;   // pinned host staging [B * min(S, HS_MAX_TOPK)][R]
+    uint8_t* ce_d_stage;   // device staging, same size
+    int32_t* ce_h_cnt;     // pinned [B]
+    int32_t* ce_h_tok;     // pinned [B][S]
+    GatherPool* ce_pool;
 };
 
 namespace {
@@ -77,6 +162,11 @@ void free_all(hs_handle* h)
     cudaFree(h->d_stage_in);
     cudaFree(h->d_stage_out);
     if (h->h_pool) cudaFreeHost(h->h_pool);
+    if (h->ce_h_stage) cudaFreeHost(h->ce_h_stage);
+    cudaFree(h->ce_d_stage);
+    if (h->ce_h_cnt) cudaFreeHost(h->ce_h_cnt);
+    if (h->ce_h_tok) cudaFreeHost(h->ce_h_tok);
+    delete h->ce_pool;
 }
 
 int fill_start_state(hs_handle* h)
@@ -196,6 +286,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
     h->copy_mode = HS_COPY_AUTO;
+    h->policy = HS_POLICY_LRU;
     const int rc = fill_start_state(h);
     if (rc != HS_OK) {
         free_all(h);
@@ -249,6 +340,7 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
     ra.R = h->R;
     ra.rows_per_group = h->copy_rows_per_group;
     ra.done = h->d_done;
+    ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
 
     const bool prof = h->prof_before && h->prof_after;
     const bool fused = h->copy_mode == HS_COPY_FUSED ||
@@ -278,9 +370,120 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
     ca.H = h->H;
     ca.rows_per_group = h->copy_rows_per_group;
     ca.advance_step = 1;
+    ca.flat_src = 0;
     if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
     if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
     if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                  hs_stream_t stream)
+{
+    if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
+    if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t B = (size_t)h->B, S = (size_t)h->S, R = (size_t)h->R;
+    if (!h->ce_pool) {
+        const size_t rows = B * (size_t)(h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK);
+        void* p = nullptr;
+        bool ok = cudaHostAlloc(&p, rows * R, cudaHostAllocDefault) == cudaSuccess;
+        h->ce_h_stage = static_cast<uint8_t*>(p);
+        ok = ok && cudaMalloc(reinterpret_cast<void**>(&h->ce_d_stage), rows * R) == cudaSuccess;
+        ok = ok && cudaHostAlloc(&p, B * sizeof(int32_t), cudaHostAllocDefault) == cudaSuccess;
+        if (ok) h->ce_h_cnt = static_cast<int32_t*>(p);
+        ok = ok && cudaHostAlloc(&p, B * S * sizeof(int32_t), cudaHostAllocDefault) == cudaSuccess;
+        if (ok) h->ce_h_tok = static_cast<int32_t*>(p);
+        if (!ok) {
+            cudaGetLastError();
+            return HS_ERR_ALLOC;
+        }
+        unsigned n = std::thread::hardware_concurrency();
+        h->ce_pool = new (std::nothrow) GatherPool(n ? (int)n : 4);
+        if (!h->ce_pool) return HS_ERR_ALLOC;
+    }
+
+    // (1)-(3) on the device: the resolve kernel writes the miss lists.
+    ResolveArgs ra = {};
+    ra.topk = topk_idx;
+    ra.out = out_slot;
+    ra.tok_slot = h->d_tok_slot;
+    ra.slot_tok = h->d_slot_tok;
+    ra.stamp = h->d_stamp;
+    ra.len = h->d_len;
+    ra.miss_tok = h->d_miss_tok;
+    ra.miss_slot = h->d_miss_slot;
+    ra.miss_cnt = h->d_miss_cnt;
+    ra.st = h->d_st;
+    ra.K = K;
+    ra.C = h->C;
+    ra.S = h->S;
+    ra.T = h->T;
+    ra.cold = h->cold;
+    ra.list_stride = h->S;
+    ra.hash_bits = hs_hash_bits(K);
+    ra.R = h->R;
+    ra.H = h->H;
+    ra.rows_per_group = 1;
+    ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
+    if (hs_launch_resolve(ra, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
+
+    // The host needs the miss tokens: one read-back and one synchronisation.
+    if (cudaMemcpyAsync(h->ce_h_cnt, h->d_miss_cnt, B * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(h->ce_h_tok, h->d_miss_tok, B * S * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    std::vector<long long> off(B + 1, 0);
+    for (size_t b = 0; b < B; ++b) off[b + 1] = off[b] + h->ce_h_cnt[b];
+    const long long M = off[B];
+
+    // Host threads gather the rows into the staging area in flattened
+    // (request, miss) order -- the order the scatter kernel expects.
+    const long long chunk = 256;
+    const int ntasks = (int)((M + chunk - 1) / chunk);
+    const uint8_t* pool = h->h_pool;
+    uint8_t* stage = h->ce_h_stage;
+    const int32_t* toks = h->ce_h_tok;
+    const long long H = h->H;
+    std::function<void(int)> gather = [&](int task) {
+        const long long r0 = (long long)task * chunk;
+        const long long r1 = r0 + chunk < M ? r0 + chunk : M;
+        size_t b = 0;
+        while (b + 1 < B && off[b + 1] <= r0) ++b;
+        for (long long r = r0; r < r1; ++r) {
+            while (off[b + 1] <= r) ++b;
+            const long long i = r - off[b];
+            const int32_t t = toks[b * S + (size_t)i];
+            std::memcpy(stage + (size_t)r * R, pool + ((long long)b * H + t) * (long long)R, R);
+        }
+    };
+    h->ce_pool->run(ntasks, gather);
+
+    // One large copy-engine transfer, then the rows go to their slots.
+    if (M > 0 && cudaMemcpyAsync(h->ce_d_stage, h->ce_h_stage, (size_t)M * R,
+                                 cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    CopyArgs ca;
+    ca.miss_cnt = h->d_miss_cnt;
+    ca.miss_tok = h->d_miss_tok;
+    ca.miss_slot = h->d_miss_slot;
+    ca.pool = h->ce_d_stage;
+    ca.buf = h->d_buf;
+    ca.st = h->d_st;
+    ca.B = h->B;
+    ca.S = h->S;
+    ca.T = h->T;
+    ca.R = h->R;
+    ca.list_stride = h->S;
+    ca.H = h->H;
+    ca.rows_per_group = h->copy_rows_per_group;
+    ca.advance_step = 1;
+    ca.flat_src = 1;
+    if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, false) != cudaSuccess) return HS_ERR_CUDA;
     return HS_OK;
 }
 
@@ -290,6 +493,13 @@ int hs_resolve_launches(hs_handle* h)
     const bool fused = h->copy_mode == HS_COPY_FUSED ||
                        (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
     return fused ? 1 : 2;
+}
+
+int hs_set_policy(hs_handle* h, int policy)
+{
+    if (!valid(h) || (policy != HS_POLICY_LRU && policy != HS_POLICY_FIFO)) return HS_ERR_ARG;
+    h->policy = policy;
+    return HS_OK;
 }
 
 int hs_set_copy_mode(hs_handle* h, int mode)
@@ -425,7 +635,8 @@ int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t*
 int hs_import_state(hs_handle* h, const int32_t* tok_slot, const int32_t* slot_tok,
                     const int32_t* stamp, int32_t step)
 {
-    if (!valid(h) || !tok_slot || !slot_tok || !stamp || step < 0) return HS_ERR_ARG;
+    if (!valid(h) || !tok_slot || !slot_tok || !stamp || step < 0 || step > HS_MAX_STEP)
+        return HS_ERR_ARG;
     const size_t C = (size_t)h->C, S = (size_t)h->S;
     for (int b = 0; b < h->B; ++b) {
         const int32_t* ts = tok_slot + (size_t)b * C;

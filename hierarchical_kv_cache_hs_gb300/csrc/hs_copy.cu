@@ -92,7 +92,9 @@ __global__ void __launch_bounds__(CT) hs_copy_kernel(CopyArgs a)
             }
             const int i = (int)(r - s_pref[lo]);
             const size_t li = (size_t)lo * a.list_stride + i;
-            src = ((long long)lo * a.H + a.miss_tok[li]) * a.R;
+            // Flat source: row r of a staging area (the copy-engine variant);
+            // otherwise token t of request lo in the host pool.
+            src = a.flat_src ? r * a.R : ((long long)lo * a.H + a.miss_tok[li]) * a.R;
             dst = ((long long)lo * slots + a.miss_slot[li]) * a.R;
         }
         const int nrows = (int)((total - r0) < G ? (total - r0) : G);

@@ -39,6 +39,7 @@ struct ResolveArgs {
     int R;
     int rows_per_group;
     unsigned* done;        // CTAs finished this call (returns to 0 after each call)
+    int fifo;              // 1: FIFO eviction (hits keep their fill stamp), 0: LRU
 };
 
 struct CopyArgs {
@@ -52,6 +53,7 @@ struct CopyArgs {
     long long H;
     int rows_per_group;    // rows a warp copies together (its lanes < rows_per_group own one row each)
     int advance_step;      // 1: block 0 advances st->step after the primary grid finished
+    int flat_src;          // 1: `pool` is a staging area holding the rows in flattened order
 };
 
 struct AppendArgs {
@@ -75,6 +77,18 @@ __host__ __device__ inline int hs_resolve_region_a_ints(int hash_bits)
     const int hc2 = 2 << hash_bits;
     const int hist = HS_AGE_SUBHIST * HS_AGE_BINS;
     return hc2 > hist ? hc2 : hist;
+}
+
+// Shared memory of the resolve kernel: region A, stamps [S], slot -> token
+// [S], miss tokens [K] (ints); miss row positions [K], victims [K] (uint16);
+// the hit bitmap [ceil(S/32)] (words).
+__host__ __device__ inline size_t hs_resolve_base_bytes(int K, int S, int hash_bits)
+{
+    const size_t ints = (size_t)hs_resolve_region_a_ints(hash_bits) + 2u * (size_t)S + (size_t)K;
+    size_t bytes = 4u * ints + 2u * 2u * (size_t)K;
+    bytes += 2u * (size_t)(K & 1);                          // keep the next word array aligned
+    bytes += 4u * (size_t)((S + 31) >> 5);
+    return bytes;
 }
 
 size_t hs_resolve_smem_bytes(int K, int S);

@@ -130,6 +130,7 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
     ra.R = row_bytes;
     ra.rows_per_group = 1;
     ra.done = nullptr;
+    ra.fifo = 0;
     if (hs_launch_resolve(ra, batch, s) != cudaSuccess) return HS_ERR_CUDA;
 
     int sms = 1;
@@ -150,6 +151,7 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
     const int unroll = hs_copy_unroll_for(row_bytes);
     ca.rows_per_group = hs_copy_rows_per_group(row_bytes, unroll);
     ca.advance_step = 1;
+    ca.flat_src = 0;
     const int grid = (sms > 0 ? sms : 1) * hs_copy_blocks_per_sm(unroll, batch);
     if (hs_launch_copy(ca, grid, unroll, s, true) != cudaSuccess) return HS_ERR_CUDA;
     return HS_OK;

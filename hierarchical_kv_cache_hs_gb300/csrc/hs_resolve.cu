@@ -28,7 +28,10 @@
 //   FUSED   the CTA then updates the tables and copies its own missing rows
 //           from the mapped host pool into the buffer (zero-copy 128-bit
 //           loads, U in flight per lane); the last CTA to finish advances the
-//           step counter.  One launch per step.
+//           step counter.  One launch per step.  (Reading the first rows into
+//           shared memory with cp.async while the victims are still chosen
+//           was measured slower: asynchronous copies from host memory are
+//           throttled, so issuing them stalled the CTA for tens of us.)
 //   !FUSED  the CTA writes the miss / victim lists to global memory for the
 //           grid-wide copy kernel (hs_copy.cu), which advances the counter.
 #include <climits>
@@ -96,6 +99,43 @@ __device__ __forceinline__ void st_v4(uint8_t* p, const uint4& v)
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (bypasses L1), and its fences.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One warp copies `nrows` rows: lane r < nrows holds row r's source and
+// destination byte offsets.  Every lane streams 16-byte chunks, U loads in
+// flight before the matching stores.
+template <int U>
+__device__ __forceinline__ void copy_row_group(const uint8_t* pool_b, uint8_t* buf_b, long long src,
+                                               long long dst, int nrows, int cpr, int lane)
+{
+    const int nch = nrows * cpr;
+    for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+        uint4 v[U];
+        long long d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int cc = c0 + u * 32 + lane;
+            const int rr = cc < nch ? cc / cpr : 0;
+            const long long s = __shfl_sync(FULL, src, rr);
+            const int off = (cc - rr * cpr) << 4;
+            d[u] = __shfl_sync(FULL, dst, rr) + off;
+            if (cc < nch) v[u] = ld_host_v4(pool_b + s + off);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int cc = c0 + u * 32 + lane;
+            if (cc < nch) st_v4(buf_b + d[u], v[u]);
+        }
+    }
+}
+
 template <bool FUSED, int U>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
 {
@@ -121,6 +161,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     int* s_mtok = s_slot_tok + S;             // [K]
     uint16_t* s_mj = reinterpret_cast<uint16_t*>(s_mtok + K);  // [K]
     uint16_t* s_vic = s_mj + K;                                 // [K]
+    unsigned* s_hitbits = reinterpret_cast<unsigned*>(s_vic + K + (K & 1));  // [ceil(S/32)]
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -140,14 +181,30 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     int tk[EMAX];
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) tk[e] = (e < E && j0 + e < K) ? g_topk[j0 + e] : -1;
-    for (int i = tid; i < S; i += NT) {
-        s_stamp[i] = g_stamp[i];
-        s_slot_tok[i] = g_slot_tok[i];
+    // The two S-entry rows go to shared memory with asynchronous 16-byte
+    // copies when they are 16-byte aligned, so all of them are in flight at
+    // once; otherwise with plain loads.
+    const bool vec_rows = (S & 3) == 0 &&
+        (((uintptr_t)g_stamp | (uintptr_t)g_slot_tok) & 15u) == 0;
+    if (vec_rows) {
+        for (int i = tid; i < (S >> 2); i += NT) {
+            cp_async16(s_stamp + 4 * i, g_stamp + 4 * i);
+            cp_async16(s_slot_tok + 4 * i, g_slot_tok + 4 * i);
+        }
+        cp_async_commit();
+    } else {
+        for (int i = tid; i < S; i += NT) {
+            s_stamp[i] = g_stamp[i];
+            s_slot_tok[i] = g_slot_tok[i];
+        }
     }
     for (int i = tid; i < hc; i += NT) {
         s_hkey[i] = -1;
         s_hj[i] = INT_MAX;
     }
+    if (a.fifo)
+        for (int i = tid; i < ((S + 31) >> 5); i += NT) s_hitbits[i] = 0u;
+    if (vec_rows) cp_async_wait_all();
     if (tid < 3) s_cnt[tid] = 0;
     __syncthreads();
 
@@ -166,13 +223,21 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 err |= HS_E_RANGE;
             } else {
                 cl[e] = C_MISS;  // valid; refined below
-                if (t < a.cold) sl[e] = g_tok_slot[t];  // in flight during the hash
+                if (t < a.cold) sl[e] = g_tok_slot[t];
             }
         }
     }
+    // Repeated indices: the first occurrence in row order wins.  A resident
+    // token claims its slot by raising the slot's stamp word to
+    // step + K - j (the largest value belongs to the smallest j); every other
+    // valid token (a miss or a tail token) goes through the hash.
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
-        if (cl[e] == C_MISS) {
+        if (cl[e] == C_MISS && sl[e] >= 0) atomicMax(&s_stamp[sl[e]], step + (K - (j0 + e)));
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        if (cl[e] == C_MISS && sl[e] < 0) {
             const int t = tk[e];
             unsigned h = ((unsigned)t * 0x9E3779B1u) >> (32 - a.hash_bits);
             for (;;) {
@@ -190,7 +255,24 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     for (int e = 0; e < EMAX; ++e) {
         const int j = j0 + e;
         if (cl[e] == C_MISS) {
-            if (s_hj[hs[e]] != j) {
+            if (sl[e] >= 0) {
+                // A repeat reads either the winner's claim or the normalised
+                // stamp; both differ from its own claim step + K - j.
+                if (s_stamp[sl[e]] != step + (K - j)) {
+                    cl[e] = C_BAD;
+                    err |= HS_E_DUP;
+                    g_out[j] = -1;
+                } else {
+                    cl[e] = C_HIT;
+                    // LRU: a hit refreshes its entry.  FIFO: the slot only
+                    // looks new while victims are chosen; its fill stamp is
+                    // kept at write-back.
+                    s_stamp[sl[e]] = step;
+                    if (a.fifo) atomicOr(&s_hitbits[sl[e] >> 5], 1u << (sl[e] & 31));
+                    g_out[j] = sl[e];
+                    ++nh;
+                }
+            } else if (s_hj[hs[e]] != j) {
                 cl[e] = C_BAD;
                 err |= HS_E_DUP;
                 g_out[j] = -1;
@@ -198,11 +280,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 cl[e] = C_TAIL;
                 g_out[j] = S + tk[e] % a.T;
                 ++ni;
-            } else if (sl[e] >= 0) {
-                cl[e] = C_HIT;
-                s_stamp[sl[e]] = step;  // a hit refreshes its LRU entry
-                g_out[j] = sl[e];
-                ++nh;
             } else {
                 ++nm;
             }
@@ -329,30 +406,51 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
         const int Q = (S + NT - 1) / NT;
         const int q0 = tid * Q;
         int nl = 0, ne = 0;
-        for (int q = 0; q < Q; ++q) {
-            const int s = q0 + q;
-            if (s < S) {
-                const int k = s_stamp[s];
-                nl += k < tau;
-                ne += k == tau;
+        const bool vec_q = (Q & 3) == 0 && q0 + Q <= S;  // 16-byte aligned, all in range
+        if (vec_q) {
+            for (int q = 0; q < Q; q += 4) {
+                const int4 k4 = *reinterpret_cast<const int4*>(s_stamp + q0 + q);
+                nl += (k4.x < tau) + (k4.y < tau) + (k4.z < tau) + (k4.w < tau);
+                ne += (k4.x == tau) + (k4.y == tau) + (k4.z == tau) + (k4.w == tau);
+            }
+        } else {
+            for (int q = 0; q < Q; ++q) {
+                const int s = q0 + q;
+                if (s < S) {
+                    const int k = s_stamp[s];
+                    nl += k < tau;
+                    ne += k == tau;
+                }
             }
         }
         int tot;
         const int packed = block_excl_scan((nl << 16) | ne, s_w, &tot);
         int lb = packed >> 16, eb = packed & 0xffff;
-        for (int q = 0; q < Q; ++q) {
-            const int s = q0 + q;
-            if (s < S) {
-                const int k = s_stamp[s];
-                // Exactly m slots qualify; the bound only keeps a corrupted
-                // stamp from writing past the list.
-                if (k < tau) {
-                    const int p = lb + (eb < need_eq ? eb : need_eq);
-                    if (p < m) s_vic[p] = (uint16_t)s;
-                    ++lb;
-                } else if (k == tau) {
-                    if (eb < need_eq && lb + eb < m) s_vic[lb + eb] = (uint16_t)s;
-                    ++eb;
+        // Exactly m slots qualify; the bounds only keep a corrupted stamp from
+        // writing past the list.
+        auto place = [&](int s, int k) {
+            if (k < tau) {
+                const int p = lb + (eb < need_eq ? eb : need_eq);
+                if (p < m) s_vic[p] = (uint16_t)s;
+                ++lb;
+            } else if (k == tau) {
+                if (eb < need_eq && lb + eb < m) s_vic[lb + eb] = (uint16_t)s;
+                ++eb;
+            }
+        };
+        if (nl | ne) {
+            if (vec_q) {
+                for (int q = 0; q < Q; q += 4) {
+                    const int4 k4 = *reinterpret_cast<const int4*>(s_stamp + q0 + q);
+                    place(q0 + q, k4.x);
+                    place(q0 + q + 1, k4.y);
+                    place(q0 + q + 2, k4.z);
+                    place(q0 + q + 3, k4.w);
+                }
+            } else {
+                for (int q = 0; q < Q; ++q) {
+                    const int s = q0 + q;
+                    if (s < S) place(s, s_stamp[s]);
                 }
             }
         }
@@ -395,31 +493,17 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                     src = (long long)t * a.R;
                     dst = (long long)v * a.R;
                 }
-                const int nrows = (m - r0) < G ? (m - r0) : G;
-                const int nch = nrows * cpr;
-                for (int c0 = 0; c0 < nch; c0 += 32 * U) {
-                    uint4 v[U];
-                    long long d[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int cc = c0 + u * 32 + lane;
-                        const int rr = cc < nch ? cc / cpr : 0;
-                        const long long s = __shfl_sync(FULL, src, rr);
-                        const int off = (cc - rr * cpr) << 4;
-                        d[u] = __shfl_sync(FULL, dst, rr) + off;
-                        if (cc < nch) v[u] = ld_host_v4(pool_b + s + off);
-                    }
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int cc = c0 + u * 32 + lane;
-                        if (cc < nch) st_v4(buf_b + d[u], v[u]);
-                    }
-                }
+                copy_row_group<U>(pool_b, buf_b, src, dst, (m - r0) < G ? (m - r0) : G, cpr, lane);
             }
         }
     }
     __syncthreads();
-    for (int i = tid; i < S; i += NT) g_stamp[i] = s_stamp[i];
+    if (a.fifo) {
+        for (int i = tid; i < S; i += NT)
+            if (!((s_hitbits[i >> 5] >> (i & 31)) & 1u)) g_stamp[i] = s_stamp[i];
+    } else {
+        for (int i = tid; i < S; i += NT) g_stamp[i] = s_stamp[i];
+    }
     if (tid == 0) {
         a.miss_cnt[b] = m;
         if (s_cnt[0]) atomicAdd(&a.st->hits, (unsigned long long)s_cnt[0]);
@@ -450,11 +534,7 @@ int hs_hash_bits(int K)
 
 size_t hs_resolve_smem_bytes(int K, int S)
 {
-    const int region_a = hs_resolve_region_a_ints(hs_hash_bits(K));
-    // ints: region A, stamps [S], slot -> token [S], miss tokens [K];
-    // uint16: miss row positions [K], victims [K]
-    return sizeof(int) * ((size_t)region_a + 2u * (size_t)S + (size_t)K) +
-           sizeof(uint16_t) * 2u * (size_t)K;
+    return hs_resolve_base_bytes(K, S, hs_hash_bits(K));
 }
 
 cudaError_t hs_prepare_resolve()

@@ -31,6 +31,9 @@ HS_E_RANGE = 1
 HS_E_DUP = 2
 HS_E_APPEND = 4
 
+HS_POLICY_LRU = 0
+HS_POLICY_FIFO = 1
+
 HS_COPY_AUTO = 0
 HS_COPY_FUSED = 1
 HS_COPY_SPLIT = 2
@@ -71,6 +74,7 @@ def _load():
         "hs_destroy": ([P], None),
         "hs_resolve": ([P, P, I, P, P], I),
         "hs_resolve_host": ([P, P, I, P, P], I),
+        "hs_resolve_ce": ([P, P, I, P, P], I),
         "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
         "hs_host_pool": ([P], P),
         "hs_host_pool_bytes": ([P], Z),
@@ -87,6 +91,7 @@ def _load():
         "hs_profile_events": ([P, P, P], I),
         "hs_set_copy_mode": ([P, I], I),
         "hs_resolve_launches": ([P], I),
+        "hs_set_policy": ([P, I], I),
         "hs_resolve_noalloc": ([I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], I),
         "hs_error_string": ([I], ctypes.c_char_p),
     }
@@ -164,6 +169,12 @@ def hs_resolve_rc(h: int, topk_idx, K: int, out_slot, stream=None) -> int:
 def hs_resolve_host(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
     _check(lib.hs_resolve_host(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream)),
            "hs_resolve_host")
+
+
+def hs_resolve_ce(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
+    """The copy-engine comparison variant (synchronises once per call)."""
+    _check(lib.hs_resolve_ce(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream)),
+           "hs_resolve_ce")
 
 
 def hs_stats(h: int, last_miss=None) -> dict:
@@ -261,6 +272,10 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
 
 def hs_set_copy_mode(h: int, mode: int) -> None:
     _check(lib.hs_set_copy_mode(h, int(mode)), "hs_set_copy_mode")
+
+
+def hs_set_policy(h: int, policy: int) -> None:
+    _check(lib.hs_set_policy(h, int(policy)), "hs_set_policy")
 
 
 def hs_resolve_launches(h: int) -> int:

@@ -89,16 +89,23 @@ class GpuWorkload:
     def out_at(self, layer: int, step: int) -> torch.Tensor:
         return self.out[layer, step] if self.record else self.out[layer]
 
-    def launch_step(self, s: int, stream=None) -> int:
-        """Enqueue step s for every layer; returns the number of kernel launches."""
+    def launch_step(self, s: int, stream=None, copy_engine: bool = False) -> int:
+        """Enqueue step s for every layer; returns the number of kernel launches.
+
+        ``copy_engine`` uses the copy-engine comparison variant (hs_resolve_ce),
+        which synchronises the stream inside every call."""
         wl = self.wl
         n = 0
         for layer, h in enumerate(self.handles):
             if self.append_rows is not None:
                 hs.hs_append(h.h, self.append_rows[layer, s], stream)
                 n += 1
-            hs.hs_resolve(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), stream)
-            n += hs.hs_resolve_launches(h.h)
+            if copy_engine:
+                hs.hs_resolve_ce(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), stream)
+                n += 2
+            else:
+                hs.hs_resolve(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), stream)
+                n += hs.hs_resolve_launches(h.h)
         return n
 
     def host_step(self, s: int, out_host: torch.Tensor, stream=None) -> None:

@@ -78,7 +78,9 @@ typedef struct CUstream_st* hs_stream_t;
 #define HS_E_DUP     2  /* an index repeated within one top-k row */
 #define HS_E_APPEND  4  /* hs_append with no room in the resident tail */
 
-/* Kernel limits. */
+/* Kernel limits.  The step counter runs up to HS_MAX_STEP (stamps and the
+ * in-kernel claim of a slot, step + K, stay below 2^31). */
+#define HS_MAX_STEP       0x7fffefff
 #define HS_MAX_TOPK       4096
 #define HS_MAX_SLOTS      16384
 #define HS_MAX_BATCH      4096
@@ -134,6 +136,20 @@ int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_s
                     hs_stream_t stream);
 
 /*
+ * Copy-engine variant of hs_resolve, kept for comparison with the zero-copy
+ * row fetch.  The resolve kernel writes the miss lists; the host reads the
+ * miss tokens back (one stream synchronisation per call), gathers the
+ * missing rows from the pinned pool into a pinned staging area with host
+ * threads, moves the whole area with one cudaMemcpyAsync, and a kernel
+ * writes every row into its victim slot.  Results are identical to
+ * hs_resolve.  Not graph-capturable.  The first call allocates the staging
+ * areas (B * min(S, HS_MAX_TOPK) rows on the host and on the device) and
+ * starts the host threads.
+ */
+int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                  hs_stream_t stream);
+
+/*
  * Read the counters and, if last_miss is not NULL, the last step's miss count
  * of every request (host, [B]).  Synchronises the device first.
  */
@@ -183,7 +199,7 @@ int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t*
  * counter.  The state is checked on the host first and refused with
  * HS_ERR_ARG unless it is one the path can reach: slot -> token entries in
  * [-1, C - T), token -> slot entries in [-1, S) and -1 for tail tokens, the
- * two maps inverse to each other, every stamp in [0, step], step >= 0.
+ * two maps inverse to each other, every stamp in [0, step], 0 <= step <= HS_MAX_STEP.
  * Buffer bytes are not part of the state (write them, or let misses refill
  * them).  Counters and error bits are cleared.  Synchronous.
  */
@@ -220,6 +236,21 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
 #define HS_COPY_SPLIT  2
 #define HS_FUSED_MIN_BATCH 16
 int hs_set_copy_mode(hs_handle* h, int mode);
+
+/*
+ * Eviction policy (HiSparse blog, "Efficient swap-in kernel": the miss count
+ * depends on the buffer size and the eviction strategy):
+ *   HS_POLICY_LRU   victims are the least recently used slots; a hit
+ *                   refreshes its slot's stamp (default);
+ *   HS_POLICY_FIFO  victims are the slots filled longest ago; a hit keeps its
+ *                   slot's fill stamp (the slot is still not evicted in the
+ *                   step that hits it).
+ * Ties go to the lowest slot index under both.  Takes effect at the next
+ * hs_resolve; switching mid-run keeps the stamps as they are.
+ */
+#define HS_POLICY_LRU   0
+#define HS_POLICY_FIFO  1
+int hs_set_policy(hs_handle* h, int policy);
 
 /* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG. */
 int hs_resolve_launches(hs_handle* h);

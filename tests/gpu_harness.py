@@ -21,9 +21,13 @@ class GpuResult:
     pass
 
 
-def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO):
+def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO,
+            policy=hs.HS_POLICY_LRU, copy_engine=False):
     """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one."""
     w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
+    for h in w.handles:
+        hs.hs_set_policy(h.h, policy)
+    res_policy = policy
     if setup is not None:
         setup(w)
     if trace is not None:
@@ -48,7 +52,7 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
     else:
         with torch.cuda.stream(stream):
             for s in range(steps):
-                w.launch_step(s, stream)
+                w.launch_step(s, stream, copy_engine=copy_engine)
                 for layer, h in enumerate(w.handles):
                     hs.hs_stats(h.h, res.misses[layer, s])
     torch.cuda.synchronize()
@@ -57,10 +61,11 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
     res.stats = [h.stats() for h in w.handles]
     res.state = [h.export_state() for h in w.handles]
     res.workload = w
+    res.policy = res_policy
     return res
 
 
-def oracle_request(wl, layer, b, trace_lb, steps):
+def oracle_request(wl, layer, b, trace_lb, steps, policy=0):
     host = tg.rows(wl, layer, b, 0, wl.cold)
     append_rows = tg.rows(wl, layer, b, wl.len0, steps) if wl.grow else None
     tail_init = None
@@ -73,7 +78,7 @@ def oracle_request(wl, layer, b, trace_lb, steps):
                 st.buf[wl.S + t % wl.T] = tail[i]
     length = wl.len0 if wl.grow else wl.C
     return oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace_lb, length=length,
-                              append_rows=append_rows, tail_init=tail_init)
+                              append_rows=append_rows, tail_init=tail_init, policy=policy)
 
 
 def compare(wl, res, requests=None, layers=None):
@@ -86,7 +91,8 @@ def compare(wl, res, requests=None, layers=None):
 
     def one(job):
         layer, b = job
-        st, outs, counts, errs = oracle_request(wl, layer, b, res.trace[layer, :, b], steps)
+        st, outs, counts, errs = oracle_request(wl, layer, b, res.trace[layer, :, b], steps,
+                                                policy=getattr(res, "policy", 0))
         tok, slot_tok, stamp, step = res.state[layer]
         ctx = "layer %d request %d" % (layer, b)
         np.testing.assert_array_equal(res.out[layer, :, b], outs, err_msg=ctx + " out_slot")

@@ -28,9 +28,9 @@ def _built():
 
 
 def _run_and_compare(wl, steps=None, requests=None, graph=False, trace=None, expect_err=0,
-                     copy_mode=0):
+                     copy_mode=0, policy=0):
     from gpu_harness import check_counters, compare, gpu_run
-    res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode)
+    res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode, policy=policy)
     try:
         tot, err = compare(wl, res, requests=requests)
         if requests is None:
@@ -165,6 +165,37 @@ def test_parity_other_launch_mode(name, mode):
     """The launch mode that the default (fused from 16 requests up) does not pick."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
     _run_and_compare(wl, copy_mode=mode)
+
+
+@pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 2),
+                                       ("tiny_b1_c8k", 0), ("b256_c32k_grow_tail512", 0),
+                                       ("ragged", 1)])
+def test_parity_fifo_policy(name, mode):
+    """FIFO eviction (hits keep their fill stamp) against the oracle's FIFO."""
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    res, tot = _run_and_compare(wl, copy_mode=mode, policy=1)
+
+
+def test_fifo_misses_more_than_lru():
+    wl = tg.WORKLOADS["b32_c32k_s4096"]
+    per = {}
+    for policy in (0, 1):
+        res, tot = _run_and_compare(wl, steps=40, policy=policy)
+        per[policy] = tot[1]
+    assert per[0] < per[1]
+
+
+@pytest.mark.parametrize("name", ["b32_c32k_s4096", "b256_c32k_grow_tail512", "ragged"])
+def test_parity_copy_engine_variant(name):
+    """hs_resolve_ce (host gather + one copy-engine transfer) against the oracle."""
+    from gpu_harness import check_counters, compare, gpu_run
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    res = gpu_run(wl, steps=min(wl.steps, 40), copy_engine=True)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+    finally:
+        res.workload.close()
 
 
 def test_resolve_host_matches_device_path():
