@@ -340,17 +340,53 @@ def run_ours(args, rank, world, dist):
     main = measure(wl, want_e2e=not args.no_e2e, want_ce=not args.no_ce)
     clocks = sampler.stop()
 
+    def policy_sweep(wl):
+        """Buffer size x eviction policy: the axes of the blog's miss-count figure."""
+        out = {}
+        w = GpuWorkload(wl, steps=total_steps, record=False, request_offset=shard_requests(rank, wl.B)[0],
+                        copy_mode=mode)
+        stream = torch.cuda.Stream(device=dev)
+        try:
+            for pname, pol in (("lru", hs.HS_POLICY_LRU), ("fifo", hs.HS_POLICY_FIFO)):
+                w.reset()
+                for h in w.handles:
+                    hs.hs_set_policy(h.h, pol)
+                import numpy as np
+                last = np.zeros(wl.B, dtype=np.int32)
+                ms, per_step = 0.0, []
+                with torch.cuda.stream(stream):
+                    for s in range(PRIME_STEPS + args.warmup):
+                        w.launch_step(s, stream)
+                    for i in range(args.steps):
+                        s = PRIME_STEPS + args.warmup + i
+                        flush.fill_(i & 0xFF)
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        w.launch_step(s, stream)
+                        e1.record(stream)
+                        e1.synchronize()
+                        ms += e0.elapsed_time(e1)
+                        tot = 0
+                        for h in w.handles:
+                            hs.hs_stats(h.h, last)
+                            tot += int(last.sum())
+                        per_step.append(tot)
+                out[pname] = {
+                    "resolves_per_s": wl.B * wl.layers * args.steps / (ms / 1e3),
+                    "ms_per_step": ms / args.steps,
+                    "miss_row_gbs": sum(per_step) * wl.row_bytes / (ms / 1e3) / 1e9,
+                    "misses_per_step_mean": statistics.mean(per_step),
+                    "misses_per_step": per_step,
+                }
+        finally:
+            w.close()
+        return out
+
     sweep = {}
     if not args.no_sweep and args.workload == "b64_c64k_s4096":
-        other = tg.WORKLOADS["b64_c64k_s2048"]
-        r2 = measure(other, want_profile=True, want_e2e=False)
-        sweep["b64_c64k_s2048"] = {
-            "resolves_per_s": other.B * other.layers * args.steps / (r2["dev_ms"] / 1e3),
-            "miss_row_gbs": r2["miss_rows"] * other.row_bytes / (r2["dev_ms"] / 1e3) / 1e9,
-            "ms_per_step": r2["dev_ms"] / args.steps,
-            "misses_per_step_mean": statistics.mean(r2["misses_per_step"]),
-            "misses_per_step": r2["misses_per_step"],
-        }
+        for name in ("b64_c64k_s4096", "b64_c64k_s2048"):
+            sweep[name] = policy_sweep(tg.WORKLOADS[name])
 
     units = wl.B * wl.layers * args.steps
     dev_s = max_over_ranks(main["dev_ms"] / 1e3)
