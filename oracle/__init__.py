@@ -59,6 +59,12 @@ def load_library(path: str):
         lib.or_resolve_policy.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
                                           i32]
         lib.or_resolve_policy.restype = i32
+    if hasattr(lib, "or_resolve_ex"):
+        lib.or_resolve_ex.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
+                                      i32, i32]
+        lib.or_resolve_ex.restype = i32
+        lib.or_append_sliding.argtypes = [i32, i32, i32, i32, P, P, P, P]
+        lib.or_append_sliding.restype = i32
     lib.or_append.argtypes = [i32, i32, i32, i32, P, P, P]
     lib.or_append.restype = i32
     return lib
@@ -76,9 +82,10 @@ class RequestState:
     """State of one request: tables, stamps, device-buffer model and length."""
 
     def __init__(self, C: int, S: int, T: int, R: int, length: Optional[int] = None, lib=None,
-                 policy: int = POLICY_LRU):
+                 policy: int = POLICY_LRU, sliding: bool = False):
         self.lib = lib if lib is not None else _lib()
         self.policy = int(policy)
+        self.sliding = bool(sliding)
         self.C, self.S, self.T, self.R = int(C), int(S), int(T), int(R)
         self.tok_slot = np.empty(C, dtype=np.int32)
         self.slot_tok = np.empty(S, dtype=np.int32)
@@ -96,6 +103,7 @@ class RequestState:
         topk = np.ascontiguousarray(topk, dtype=np.int32)
         assert host.dtype == np.uint8 and host.flags.c_contiguous
         assert host.shape[0] >= self.C - self.T and host.shape[1] == self.R
+        self.host = host  # a sliding tail writes rows back into it
         out = np.empty(topk.shape[0], dtype=np.int32)
         counts = np.zeros(3, dtype=np.int32)
         args = (self.C, self.S, self.T, self.R, int(self.len[0]),
@@ -103,16 +111,27 @@ class RequestState:
                 self.stamp.ctypes.data, self.buf.ctypes.data, host.ctypes.data,
                 topk.ctypes.data, int(topk.shape[0]), int(step),
                 out.ctypes.data, counts.ctypes.data)
-        if self.policy == POLICY_LRU:
+        if self.sliding:
+            err = self.lib.or_resolve_ex(*args, self.policy, 1)
+        elif self.policy == POLICY_LRU:
             err = self.lib.or_resolve(*args)
         else:
             err = self.lib.or_resolve_policy(*args, self.policy)
         return out, (int(counts[0]), int(counts[1]), int(counts[2])), int(err)
 
-    def append(self, row: np.ndarray) -> int:
-        """Write the next token's row into the resident tail; returns error bits."""
+    def append(self, row: np.ndarray, host: Optional[np.ndarray] = None) -> int:
+        """Write the next token's row into the resident tail; returns error bits.
+
+        With a sliding tail, the token leaving the tail is written back into
+        ``host`` (uint8 [C-T][R], the request's host rows)."""
         row = np.ascontiguousarray(row, dtype=np.uint8)
         assert row.shape == (self.R,)
+        if self.sliding:
+            assert host is not None and host.dtype == np.uint8 and host.flags.c_contiguous
+            assert host.shape[0] >= self.C - self.T and host.shape[1] == self.R
+            return int(self.lib.or_append_sliding(self.C, self.S, self.T, self.R,
+                                                  self.len.ctypes.data, self.buf.ctypes.data,
+                                                  host.ctypes.data, row.ctypes.data))
         return int(self.lib.or_append(self.C, self.S, self.T, self.R, self.len.ctypes.data,
                                     self.buf.ctypes.data, row.ctypes.data))
 
@@ -120,7 +139,7 @@ class RequestState:
 def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.ndarray,
                 length: Optional[int] = None, append_rows: Optional[np.ndarray] = None,
                 tail_init: Optional[Callable[[RequestState], None]] = None,
-                step0: int = 0, policy: int = POLICY_LRU):
+                step0: int = 0, policy: int = POLICY_LRU, sliding: bool = False):
     """Replay ``topk_rows`` [steps][K] for one request from the empty state.
 
     ``append_rows`` [steps][R], when given, is appended before each step's
@@ -128,7 +147,7 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
     (state, out [steps][K], counts [steps][3], resolve error bits [steps]);
     ``state.append_errs`` holds the OR of the appends' error bits.
     """
-    st = RequestState(C, S, T, R, length, policy=policy)
+    st = RequestState(C, S, T, R, length, policy=policy, sliding=sliding)
     st.append_errs = 0
     if tail_init is not None:
         tail_init(st)
@@ -138,7 +157,7 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
     errs = np.empty(steps, dtype=np.int32)
     for s in range(steps):
         if append_rows is not None:
-            st.append_errs |= st.append(append_rows[s])
+            st.append_errs |= st.append(append_rows[s], host)
         o, c, e = st.resolve(host, topk_rows[s], step0 + s + 1)
         outs[s] = o
         counts[s] = c

@@ -26,6 +26,16 @@
  * alternative: a slot's stamp is the step it was filled, hits do not refresh
  * it, and a slot hit in this step is still never evicted in that step.
  *
+ * Resident tail, two readings of which tokens it holds:
+ *   fixed    the last T positions of the capacity, [C - T, C) (a growing
+ *            context appends into it until it is full);
+ *   sliding  the last T tokens written, [len - T, len): a token that leaves
+ *            the tail on an append is written back to its host row and from
+ *            then on is an ordinary host-backed token (vLLM Hybrid HiSparse
+ *            post, "Full Residency" and "Mixed Residency": the tail stays on
+ *            the GPU while older pages move to host memory, copied there so
+ *            that eviction needs no further copy).
+ *
  * Readings where the pages are silent (each is a plain choice):
  *   - one token per page: the table maps token -> slot;
  *   - a stamp is the step counter at last use (hit or fill); steps start
@@ -95,14 +105,15 @@ void or_init(int32_t C, int32_t S, int32_t* tok_slot, int32_t* slot_tok, int32_t
  *
  * Returns the error bits (OR_E_*).
  */
-int32_t or_resolve_policy(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
-                          int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
-                          const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
-                          int32_t* out, int32_t* counts, int32_t policy)
+int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                      int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                      const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                      int32_t* out, int32_t* counts, int32_t policy, int32_t sliding)
 {
     int32_t err = 0;
     int32_t hits = 0, nmiss = 0, inplace = 0;
-    const int32_t cold = C - T;
+    /* First position of the resident tail. */
+    const int32_t cold = sliding ? (len - T > 0 ? len - T : 0) : C - T;
 
     unsigned char* seen = (unsigned char*)calloc((size_t)(C > 0 ? C : 1), 1);
     unsigned char* hit = (unsigned char*)calloc((size_t)(S > 0 ? S : 1), 1);
@@ -178,6 +189,16 @@ int32_t or_resolve_policy(int32_t C, int32_t S, int32_t T, int32_t R, int32_t le
     return err;
 }
 
+/* Fixed tail, chosen eviction policy. */
+int32_t or_resolve_policy(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                          int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                          const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                          int32_t* out, int32_t* counts, int32_t policy)
+{
+    return or_resolve_ex(C, S, T, R, len, tok_slot, slot_tok, stamp, buf, host, topk, K, step,
+                         out, counts, policy, 0);
+}
+
 /* The LRU step (the swap-in kernel's policy). */
 int32_t or_resolve(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
                    int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
@@ -200,6 +221,24 @@ int32_t or_append(int32_t C, int32_t S, int32_t T, int32_t R, int32_t* len,
     int32_t t = *len;
     if (T <= 0 || t < C - T || t >= C) return OR_E_RANGE;
     memcpy(buf + (size_t)(S + t % T) * (size_t)R, row, (size_t)R);
+    *len = t + 1;
+    return 0;
+}
+
+/*
+ * Sliding tail: append token *len.  When the tail already holds T tokens, the
+ * oldest one (position *len - T, in the same tail slot) is first written back
+ * to its host row.  Only a token below the capacity C can be appended;
+ * otherwise nothing changes and OR_E_RANGE is returned.
+ */
+int32_t or_append_sliding(int32_t C, int32_t S, int32_t T, int32_t R, int32_t* len,
+                          uint8_t* buf, uint8_t* host, const uint8_t* row)
+{
+    int32_t t = *len;
+    if (T <= 0 || t >= C) return OR_E_RANGE;
+    uint8_t* slot = buf + (size_t)(S + t % T) * (size_t)R;
+    if (t >= T) memcpy(host + (size_t)(t - T) * (size_t)R, slot, (size_t)R);
+    memcpy(slot, row, (size_t)R);
     *len = t + 1;
     return 0;
 }

@@ -17,6 +17,8 @@ mismatch:
   - with ``fifo=True`` only refilled slots move to the most-recent end: hits
     leave the order alone (first in, first out), but a slot hit in this step
     is still skipped as a victim.
+  - with ``sliding=True`` the tail holds the last T tokens written; an append
+    copies the leaving token's tail row into ``host_store`` first.
 
 Semantics: HiSparse blog, "Efficient swap-in kernel" (miss detection, LRU
 eviction, page-table update + host fetch); vLLM Hybrid HiSparse post, "Mixed
@@ -25,9 +27,12 @@ Residency" (tail read in place, hits refresh LRU, one row per miss).
 
 
 class LinkedLRU:
-    def __init__(self, S, T, C, length, host_row, tail_row=None, fifo=False):
+    def __init__(self, S, T, C, length, host_row, tail_row=None, fifo=False, sliding=False,
+                 host_store=None):
         self.S, self.T, self.C, self.len = S, T, C, length
         self.fifo = fifo
+        self.sliding = sliding
+        self.host_store = host_store
         self.host_row = host_row          # token -> bytes
         self.content = [None] * S         # token held by each slot
         self.buf = [None] * (S + T)       # bytes per slot
@@ -67,6 +72,16 @@ class LinkedLRU:
 
     def append(self, row):
         t = self.len
+        if self.sliding:
+            if self.T <= 0 or t >= self.C:
+                return 1
+            if t >= self.T:
+                old = self.buf[self.S + t % self.T]
+                if old is not None:
+                    self.host_store[t - self.T] = old
+            self.buf[self.S + t % self.T] = row
+            self.len = t + 1
+            return 0
         if self.T <= 0 or t < self.C - self.T or t >= self.C:
             return 1
         self.buf[self.S + t % self.T] = row
@@ -75,6 +90,7 @@ class LinkedLRU:
 
     def step(self, topk):
         S, T, C = self.S, self.T, self.C
+        tail0 = max(self.len - T, 0) if self.sliding else C - T
         out = [-1] * len(topk)
         err = 0
         hits, misses, inplace = [], [], 0
@@ -87,7 +103,7 @@ class LinkedLRU:
             if any(topk[i] == t for i in range(j)):
                 err |= 2
                 continue
-            if t >= C - T:
+            if t >= tail0:
                 out[j] = S + t % T
                 inplace += 1
                 continue

@@ -60,12 +60,14 @@ def _parse_golden():
 
 def check_golden(oracle_mod, lib=None):
     cases = _parse_golden()
-    assert [c["name"] for c in cases] == ["A", "B", "F"]
+    assert [c["name"] for c in cases] == ["A", "B", "F", "S"]
     R = 16
     for case in cases:
         S, K, C, T, L = case["S"], case["K"], case["C"], case["T"], case["len"]
+        sliding = bool(case.get("sliding", 0))
         host = _host_rows(C, T, R)
-        st = oracle_mod.RequestState(C, S, T, R, L, lib=lib, policy=case.get("policy", 0))
+        st = oracle_mod.RequestState(C, S, T, R, L, lib=lib, policy=case.get("policy", 0),
+                                     sliding=sliding)
         tail_rows = {}
         for t in case["tail"]:
             row = np.full(R, 200 + t, dtype=np.uint8)
@@ -76,7 +78,7 @@ def check_golden(oracle_mod, lib=None):
             if op[0] == "append":
                 t = int(st.len[0])
                 row = np.full(R, 200 + t, dtype=np.uint8)
-                assert st.append(row) == 0
+                assert st.append(row, host) == 0
                 tail_rows[t] = row
                 continue
             _, n, topk, out, slot_tok, stamp, counts, err = op
@@ -95,11 +97,16 @@ def check_golden(oracle_mod, lib=None):
                 if t >= 0:
                     inv[t] = s
             assert st.tok_slot.tolist() == inv.tolist()
+            # a token that went through the tail carries its tail bytes (200 + t)
             for s, t in enumerate(slot_tok):
                 if t >= 0:
-                    assert (st.buf[s] == t).all()
-            for t, row in tail_rows.items():
-                assert (st.buf[S + t % T] == row).all()
+                    assert (st.buf[s] == (200 + t if t in tail_rows else t)).all(), (case["name"], n)
+            live = sorted(tail_rows)[-T:] if sliding else sorted(tail_rows)
+            for t in live:
+                assert (st.buf[S + t % T] == tail_rows[t]).all()
+            if sliding:  # written back: every token that left the tail
+                for t in sorted(tail_rows)[:-T] if len(tail_rows) > T else []:
+                    assert (host[t] == 200 + t).all()
 
 
 def test_golden_hand_example(oracle_lib):
@@ -148,19 +155,32 @@ def _random_row(rng, K, length, prev, p_bad):
     return row
 
 
-def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False):
+def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False, sliding=False):
     R = 8
     for seed in seeds:
         rng = random.Random(seed)
         S, K, T, C, length, grow, steps = _random_case(rng)
+        if sliding:
+            if T == 0:
+                T = rng.randint(1, 6)
+                C += T
+            grow, length = True, rng.randint(0, C - 1)
         host = _host_rows(C, T, R)
-        st = oracle_mod.RequestState(C, S, T, R, length, lib=lib, policy=1 if fifo else 0)
-        sim = LinkedLRU(S, T, C, length, host_row=lambda t: host[t].copy(), fifo=fifo)
+        host_sim = host.copy()
+        st = oracle_mod.RequestState(C, S, T, R, length, lib=lib, policy=1 if fifo else 0,
+                                     sliding=sliding)
+        sim = LinkedLRU(S, T, C, length, host_row=lambda t: host_sim[t].copy(), fifo=fifo,
+                        sliding=sliding, host_store=host_sim)
+        if sliding:  # the tail starts with the last T tokens written
+            for t in range(max(0, length - T), length):
+                row = np.full(R, (150 + t) % 256, dtype=np.uint8)
+                st.buf[S + t % T] = row
+                sim.buf[S + t % T] = row.copy()
         prev = None
         for s in range(1, steps + 1):
             if grow and rng.random() < 0.7:
                 row_bytes = np.full(R, 100 + (st.len[0] % 100), dtype=np.uint8)
-                e1 = st.append(row_bytes)
+                e1 = st.append(row_bytes, host)
                 e2 = sim.append(row_bytes)
                 assert (e1 != 0) == (e2 != 0)
             topk = _random_row(rng, K, int(st.len[0]), prev, p_bad=0.15)
@@ -183,6 +203,12 @@ def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False):
 @pytest.mark.parametrize("seed_block", range(4))
 def test_oracle_matches_linked_list_lru(oracle_lib, seed_block):
     check_against_simulator(oracle_lib, range(seed_block * 600, (seed_block + 1) * 600))
+
+
+def test_oracle_sliding_tail_matches_linked_list(oracle_lib):
+    """Sliding tail: tokens leave the tail into their host rows."""
+    check_against_simulator(oracle_lib, range(7000, 7800), sliding=True)
+    check_against_simulator(oracle_lib, range(8000, 8300), sliding=True, fifo=True)
 
 
 def test_oracle_fifo_matches_linked_list(oracle_lib):

@@ -33,6 +33,9 @@ MUTANTS = {
     "tail_offset_from_start": ("out[j] = S + t % T;", "out[j] = S + (t - cold);"),
     "tail_counted_as_miss": ("            inplace += 1;\n", "\n"),
     "stamp_plus_one": ("if (hit[s]) stamp[s] = step;", "if (hit[s]) stamp[s] = step + 1;"),
+    "fifo_refreshes_hits": ("if (policy == OR_POLICY_LRU)\n", "if (1)\n"),
+    "sliding_no_write_back": ("if (t >= T) memcpy(host", "if (0) memcpy(host"),
+    "sliding_fixed_boundary": ("sliding ? (len - T > 0 ? len - T : 0) : C - T", "C - T"),
 }
 
 
