@@ -65,6 +65,10 @@ def load_library(path: str):
         lib.or_resolve_ex.restype = i32
         lib.or_append_sliding.argtypes = [i32, i32, i32, i32, P, P, P, P]
         lib.or_append_sliding.restype = i32
+    if hasattr(lib, "or_resolve_full"):
+        lib.or_resolve_full.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
+                                        i32, i32, i32]
+        lib.or_resolve_full.restype = i32
     lib.or_append.argtypes = [i32, i32, i32, i32, P, P, P]
     lib.or_append.restype = i32
     return lib
@@ -95,10 +99,12 @@ class RequestState:
         self.lib.or_init(self.C, self.S, self.tok_slot.ctypes.data, self.slot_tok.ctypes.data,
                        self.stamp.ctypes.data)
 
-    def resolve(self, host: np.ndarray, topk: np.ndarray, step: int):
+    def resolve(self, host: np.ndarray, topk: np.ndarray, step: int, alias: bool = False):
         """Resolve one top-k row at ``step``; host is uint8 [C-T][R] by token.
 
-        Returns (out int32 [K], (hits, misses, inplace), err_bits).
+        ``alias``: the row is several positions' rows concatenated, and a
+        repeated token takes its first occurrence's slot instead of being an
+        error.  Returns (out int32 [K], (hits, misses, inplace), err_bits).
         """
         topk = np.ascontiguousarray(topk, dtype=np.int32)
         assert host.dtype == np.uint8 and host.flags.c_contiguous
@@ -111,7 +117,9 @@ class RequestState:
                 self.stamp.ctypes.data, self.buf.ctypes.data, host.ctypes.data,
                 topk.ctypes.data, int(topk.shape[0]), int(step),
                 out.ctypes.data, counts.ctypes.data)
-        if self.sliding:
+        if alias:
+            err = self.lib.or_resolve_full(*args, self.policy, 1 if self.sliding else 0, 1)
+        elif self.sliding:
             err = self.lib.or_resolve_ex(*args, self.policy, 1)
         elif self.policy == POLICY_LRU:
             err = self.lib.or_resolve(*args)

@@ -36,6 +36,13 @@
  *            the GPU while older pages move to host memory, copied there so
  *            that eviction needs no further copy).
  *
+ * Several draft positions (speculative decoding; vLLM Hybrid HiSparse post,
+ * "Speculative Decoding": a per-step resolver plan over the request's shared
+ * hot state): the P top-k rows of one step are resolved as one concatenated
+ * row.  In this "alias" mode a repeated token is not an error: it gets the
+ * slot of its first occurrence, and only first occurrences are counted,
+ * fetched and paired with victims.
+ *
  * Readings where the pages are silent (each is a plain choice):
  *   - one token per page: the table maps token -> slot;
  *   - a stamp is the step counter at last use (hit or fill); steps start
@@ -105,10 +112,11 @@ void or_init(int32_t C, int32_t S, int32_t* tok_slot, int32_t* slot_tok, int32_t
  *
  * Returns the error bits (OR_E_*).
  */
-int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
-                      int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
-                      const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
-                      int32_t* out, int32_t* counts, int32_t policy, int32_t sliding)
+int32_t or_resolve_full(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                        int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                        const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                        int32_t* out, int32_t* counts, int32_t policy, int32_t sliding,
+                        int32_t alias)
 {
     int32_t err = 0;
     int32_t hits = 0, nmiss = 0, inplace = 0;
@@ -116,6 +124,8 @@ int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
     const int32_t cold = sliding ? (len - T > 0 ? len - T : 0) : C - T;
 
     unsigned char* seen = (unsigned char*)calloc((size_t)(C > 0 ? C : 1), 1);
+    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+    int32_t* alias_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
     unsigned char* hit = (unsigned char*)calloc((size_t)(S > 0 ? S : 1), 1);
     int32_t* miss_tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
     int32_t* miss_pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
@@ -128,8 +138,14 @@ int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
         out[j] = -1;
         if (t == -1) continue;                       /* padding */
         if (t < -1 || t >= len || t >= C) { err |= OR_E_RANGE; continue; }
-        if (seen[t]) { err |= OR_E_DUP; continue; }  /* repeat of an earlier entry */
+        if (seen[t]) {                               /* repeat of an earlier entry */
+            if (alias) alias_of[j] = first[t];
+            else err |= OR_E_DUP;
+            continue;
+        }
         seen[t] = 1;
+        first[t] = j;
+        alias_of[j] = -1;
         if (t >= cold) {                             /* resident tail: in place */
             out[j] = S + t % T;
             inplace += 1;
@@ -181,12 +197,28 @@ int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
         memcpy(buf + (size_t)v * (size_t)R, host + (size_t)t * (size_t)R, (size_t)R);
     }
 
+    /* Repeats (alias mode) take their first occurrence's slot. */
+    if (alias)
+        for (int32_t j = 0; j < K; ++j) {
+            int32_t t = topk[j];
+            if (t >= 0 && t < len && t < C && seen[t] && first[t] != j) out[j] = out[alias_of[j]];
+        }
+
     counts[0] = hits;
     counts[1] = nmiss;
     counts[2] = inplace;
 
-    free(seen); free(hit); free(miss_tok); free(miss_pos); free(cand); free(victims);
+    free(seen); free(first); free(alias_of); free(hit); free(miss_tok); free(miss_pos); free(cand); free(victims);
     return err;
+}
+
+int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                      int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                      const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                      int32_t* out, int32_t* counts, int32_t policy, int32_t sliding)
+{
+    return or_resolve_full(C, S, T, R, len, tok_slot, slot_tok, stamp, buf, host, topk, K, step,
+                           out, counts, policy, sliding, 0);
 }
 
 /* Fixed tail, chosen eviction policy. */

@@ -69,16 +69,21 @@ def oracle_request(wl, layer, b, trace_lb, steps, policy=0):
     host = tg.rows(wl, layer, b, 0, wl.cold)
     append_rows = tg.rows(wl, layer, b, wl.len0, steps) if wl.grow else None
     tail_init = None
-    if wl.T > 0 and not wl.grow:
-        tail = tg.rows(wl, layer, b, wl.cold, wl.T)
+    if wl.T > 0 and (wl.sliding or not wl.grow):
+        first = max(wl.len0 - wl.T, 0) if wl.sliding else wl.cold
+        last = wl.len0 if wl.sliding else wl.C
+        tail = tg.rows(wl, layer, b, first, last - first)
 
-        def tail_init(st, tail=tail):
-            for i in range(wl.T):
-                t = wl.cold + i
+        def tail_init(st, tail=tail, first=first):
+            for i in range(tail.shape[0]):
+                t = first + i
                 st.buf[wl.S + t % wl.T] = tail[i]
-    length = wl.len0 if wl.grow else wl.C
-    return oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace_lb, length=length,
-                              append_rows=append_rows, tail_init=tail_init, policy=policy)
+    length = wl.len0 if (wl.grow or wl.sliding) else wl.C
+    st, outs, counts, errs = oracle.run_request(
+        wl.C, wl.S, wl.T, wl.row_bytes, host, trace_lb, length=length, append_rows=append_rows,
+        tail_init=tail_init, policy=policy, sliding=wl.sliding)
+    st.host_rows = host
+    return st, outs, counts, errs
 
 
 def compare(wl, res, requests=None, layers=None):
@@ -107,9 +112,16 @@ def compare(wl, res, requests=None, layers=None):
         np.testing.assert_array_equal(buf[occ], st.buf[occ], err_msg=ctx + " buffer bytes")
         if wl.T > 0:
             last = int(st.len[0])
-            toks = np.arange(wl.cold, last)
+            first = max(last - wl.T, 0) if wl.sliding else wl.cold
+            toks = np.arange(first, last)
             tslots = wl.S + toks % wl.T
             np.testing.assert_array_equal(buf[tslots], st.buf[tslots], err_msg=ctx + " tail bytes")
+        if wl.sliding:
+            # rows written back to the host pool by the appends
+            pool = res.workload.handles[layer].host_pool()[b]
+            lo, hi = max(wl.len0 - wl.T, 0), max(int(st.len[0]) - wl.T, 0)
+            np.testing.assert_array_equal(pool[lo:hi], st.host_rows[lo:hi],
+                                          err_msg=ctx + " written-back host rows")
         return counts.sum(axis=0), int(np.bitwise_or.reduce(errs)) if len(errs) else 0
 
     results = oracle.parallel_map(one, jobs)

@@ -19,6 +19,8 @@ mismatch:
     is still skipped as a victim.
   - with ``sliding=True`` the tail holds the last T tokens written; an append
     copies the leaving token's tail row into ``host_store`` first.
+  - with ``alias=True`` a repeated token is not an error: it takes the slot of
+    its first occurrence (several draft positions resolved together).
 
 Semantics: HiSparse blog, "Efficient swap-in kernel" (miss detection, LRU
 eviction, page-table update + host fetch); vLLM Hybrid HiSparse post, "Mixed
@@ -28,7 +30,8 @@ Residency" (tail read in place, hits refresh LRU, one row per miss).
 
 class LinkedLRU:
     def __init__(self, S, T, C, length, host_row, tail_row=None, fifo=False, sliding=False,
-                 host_store=None):
+                 host_store=None, alias=False):
+        self.alias = alias
         self.S, self.T, self.C, self.len = S, T, C, length
         self.fifo = fifo
         self.sliding = sliding
@@ -94,14 +97,19 @@ class LinkedLRU:
         out = [-1] * len(topk)
         err = 0
         hits, misses, inplace = [], [], 0
+        repeats = []
         for j, t in enumerate(topk):
             if t == -1:
                 continue
             if t < -1 or t >= self.len or t >= C:
                 err |= 1
                 continue
-            if any(topk[i] == t for i in range(j)):
-                err |= 2
+            earlier = [i for i in range(j) if topk[i] == t]
+            if earlier:
+                if self.alias:
+                    repeats.append((j, earlier[0]))
+                else:
+                    err |= 2
                 continue
             if t >= tail0:
                 out[j] = S + t % T
@@ -126,6 +134,8 @@ class LinkedLRU:
             self.content[v] = t
             self.buf[v] = self.host_row(t)
             out[j] = v
+        for j, i in repeats:
+            out[j] = out[i]
         touched = sorted(set(victims) if self.fifo else hit_set | set(victims))
         for s in touched:
             self._unlink(s)

@@ -100,6 +100,23 @@ def test_parity_edge_sizes(name):
     _run_and_compare(EDGE[name])
 
 
+SLIDE = tg.Workload("slide_b16_c8k_tail256", 89, B=16, C=8192, K=512, S=1024, T=256,
+                    host_ratio=8, layers=1, steps=600, len0=4096, grow=1, carry_pct=60,
+                    zipf_pct=30, third=tg.THIRD_RECENT, recent=1024, sliding=True)
+
+
+@pytest.mark.parametrize("mode,policy", [(0, 0), (2, 0), (1, 1)])
+def test_parity_sliding_tail(mode, policy):
+    """A sliding tail: tokens that leave it are written back to the host pool
+    and later come back through the hot buffer as ordinary misses."""
+    res, tot = _run_and_compare(SLIDE, copy_mode=mode, policy=policy)
+    assert tot[2] > 0 and tot[1] > 0
+
+
+def test_parity_sliding_tail_graph():
+    _run_and_compare(SLIDE, steps=64, graph=True, requests=[0, 7, 15])
+
+
 def test_parity_tail_overflow():
     """A growing context that outruns its 16-token tail: appends past the tail
     latch HS_E_APPEND, indices past the length latch HS_E_RANGE."""

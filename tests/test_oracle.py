@@ -60,7 +60,7 @@ def _parse_golden():
 
 def check_golden(oracle_mod, lib=None):
     cases = _parse_golden()
-    assert [c["name"] for c in cases] == ["A", "B", "F", "S"]
+    assert [c["name"] for c in cases] == ["A", "B", "F", "S", "M"]
     R = 16
     for case in cases:
         S, K, C, T, L = case["S"], case["K"], case["C"], case["T"], case["len"]
@@ -85,7 +85,7 @@ def check_golden(oracle_mod, lib=None):
             step += 1
             assert n == step
             assert len(topk) == K
-            o, c, e = st.resolve(host, np.array(topk), step)
+            o, c, e = st.resolve(host, np.array(topk), step, alias=bool(case.get("alias", 0)))
             assert o.tolist() == out, (case["name"], n)
             assert st.slot_tok.tolist() == slot_tok, (case["name"], n)
             assert st.stamp.tolist() == stamp, (case["name"], n)
@@ -155,7 +155,7 @@ def _random_row(rng, K, length, prev, p_bad):
     return row
 
 
-def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False, sliding=False):
+def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False, sliding=False, alias=False):
     R = 8
     for seed in seeds:
         rng = random.Random(seed)
@@ -170,7 +170,7 @@ def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False, sliding=Fal
         st = oracle_mod.RequestState(C, S, T, R, length, lib=lib, policy=1 if fifo else 0,
                                      sliding=sliding)
         sim = LinkedLRU(S, T, C, length, host_row=lambda t: host_sim[t].copy(), fifo=fifo,
-                        sliding=sliding, host_store=host_sim)
+                        sliding=sliding, host_store=host_sim, alias=alias)
         if sliding:  # the tail starts with the last T tokens written
             for t in range(max(0, length - T), length):
                 row = np.full(R, (150 + t) % 256, dtype=np.uint8)
@@ -184,8 +184,12 @@ def check_against_simulator(oracle_mod, seeds, lib=None, fifo=False, sliding=Fal
                 e2 = sim.append(row_bytes)
                 assert (e1 != 0) == (e2 != 0)
             topk = _random_row(rng, K, int(st.len[0]), prev, p_bad=0.15)
+            if alias and K > 1:  # a second position repeating some of the first's tokens
+                half = K // 2
+                topk = topk[:half] + [topk[rng.randrange(half)] if rng.random() < 0.4 else t
+                                      for t in topk[half:]]
             prev = topk
-            o, c, e = st.resolve(host, np.array(topk), s)
+            o, c, e = st.resolve(host, np.array(topk), s, alias=alias)
             so, sc, se = sim.step(topk)
             ctx = (seed, s)
             assert o.tolist() == so, ctx
@@ -209,6 +213,11 @@ def test_oracle_sliding_tail_matches_linked_list(oracle_lib):
     """Sliding tail: tokens leave the tail into their host rows."""
     check_against_simulator(oracle_lib, range(7000, 7800), sliding=True)
     check_against_simulator(oracle_lib, range(8000, 8300), sliding=True, fifo=True)
+
+
+def test_oracle_alias_matches_linked_list(oracle_lib):
+    """Several positions in one step: repeats share their first occurrence's slot."""
+    check_against_simulator(oracle_lib, range(9000, 9800), alias=True)
 
 
 def test_oracle_fifo_matches_linked_list(oracle_lib):

@@ -36,6 +36,7 @@ MUTANTS = {
     "fifo_refreshes_hits": ("if (policy == OR_POLICY_LRU)\n", "if (1)\n"),
     "sliding_no_write_back": ("if (t >= T) memcpy(host", "if (0) memcpy(host"),
     "sliding_fixed_boundary": ("sliding ? (len - T > 0 ? len - T : 0) : C - T", "C - T"),
+    "alias_repeats_unresolved": ("out[j] = out[alias_of[j]];", "out[j] = -1;"),
 }
 
 
