@@ -28,7 +28,8 @@ MUTANTS = {
     "evicted_token_kept": ("if (old >= 0) tok_slot[old] = -1;", "(void)old;"),
     "fill_not_stamped": ("        stamp[v] = step;\n", "\n"),
     "wrong_row_copied": ("host + (size_t)t * (size_t)R", "host + (size_t)v * (size_t)R"),
-    "duplicates_accepted": ("if (seen[t]) { err |= OR_E_DUP; continue; }", ""),
+    "duplicates_accepted": ("if (seen[t]) {                               /* repeat", "if (0) {  /* repeat"),
+    "duplicates_not_flagged": ("            else err |= OR_E_DUP;\n", "\n"),
     "range_off_by_one": ("t >= len || t >= C", "t > len || t >= C"),
     "tail_offset_from_start": ("out[j] = S + t % T;", "out[j] = S + (t - cold);"),
     "tail_counted_as_miss": ("            inplace += 1;\n", "\n"),
