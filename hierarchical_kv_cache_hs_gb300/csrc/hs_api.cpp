@@ -108,6 +108,7 @@ struct hs_handle {
     cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
     int copy_mode;         // HS_COPY_*
     int policy;            // HS_POLICY_*
+    int tail_mode;         // HS_TAIL_*
     int copy_grid;
     int copy_unroll;
     int copy_rows_per_group;
@@ -287,6 +288,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
     h->copy_mode = HS_COPY_AUTO;
     h->policy = HS_POLICY_LRU;
+    h->tail_mode = HS_TAIL_FIXED;
     const int rc = fill_start_state(h);
     if (rc != HS_OK) {
         free_all(h);
@@ -307,8 +309,27 @@ void hs_destroy(hs_handle* h)
     delete h;
 }
 
+static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                        hs_stream_t stream, int alias);
+
 int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                hs_stream_t stream)
+{
+    return resolve_impl(h, topk_idx, K, out_slot, stream, 0);
+}
+
+int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_t* out_slot,
+                     hs_stream_t stream)
+{
+    if (!valid(h) || P <= 0 || K <= 0) return HS_ERR_ARG;
+    const long long PK = (long long)P * K;
+    if (PK > h->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (PK > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    return resolve_impl(h, topk_idx, (int)PK, out_slot, stream, 1);
+}
+
+static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                        hs_stream_t stream, int alias)
 {
     if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
     if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
@@ -341,6 +362,8 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
     ra.rows_per_group = h->copy_rows_per_group;
     ra.done = h->d_done;
     ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
+    ra.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
+    ra.alias = alias;
 
     const bool prof = h->prof_before && h->prof_after;
     const bool fused = h->copy_mode == HS_COPY_FUSED ||
@@ -428,6 +451,8 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
     ra.H = h->H;
     ra.rows_per_group = 1;
     ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
+    ra.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
+    ra.alias = 0;
     if (hs_launch_resolve(ra, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
 
     // The host needs the miss tokens: one read-back and one synchronisation.
@@ -493,6 +518,14 @@ int hs_resolve_launches(hs_handle* h)
     const bool fused = h->copy_mode == HS_COPY_FUSED ||
                        (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
     return fused ? 1 : 2;
+}
+
+int hs_set_tail_mode(hs_handle* h, int mode)
+{
+    if (!valid(h) || (mode != HS_TAIL_FIXED && mode != HS_TAIL_SLIDING)) return HS_ERR_ARG;
+    if (mode == HS_TAIL_SLIDING && h->T <= 0) return HS_ERR_ARG;
+    h->tail_mode = mode;
+    return HS_OK;
 }
 
 int hs_set_policy(hs_handle* h, int policy)
@@ -581,6 +614,9 @@ int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream)
     a.R = h->R;
     a.C = h->C;
     a.cold = h->cold;
+    a.pool = h->d_pool;
+    a.H = h->H;
+    a.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
     if (hs_launch_append(a, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
     return HS_OK;
 }
@@ -588,7 +624,8 @@ int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream)
 int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t* rows_host)
 {
     if (!valid(h) || !rows_host || b < 0 || b >= h->B || n < 0 || h->T <= 0) return HS_ERR_ARG;
-    if (first_token < h->cold || (long long)first_token + n > h->C) return HS_ERR_ARG;
+    const int lowest = h->tail_mode == HS_TAIL_SLIDING ? 0 : h->cold;
+    if (first_token < lowest || (long long)first_token + n > h->C) return HS_ERR_ARG;
     DeviceGuard g(h->device);
     if (sync_last(h) != HS_OK) return HS_ERR_CUDA;
     const size_t R = (size_t)h->R;

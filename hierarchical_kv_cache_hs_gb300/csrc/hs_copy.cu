@@ -125,12 +125,21 @@ __global__ void hs_append_kernel(AppendArgs a)
 {
     const int b = blockIdx.x;
     const int len = a.len[b];
-    const bool ok = a.T > 0 && len >= a.cold && len < a.C;
+    const bool ok = a.T > 0 && len < a.C && (a.sliding || len >= a.cold);
     if (ok) {
         const uint4* src = reinterpret_cast<const uint4*>(a.rows + (size_t)b * a.R);
         uint4* dst = reinterpret_cast<uint4*>(
             a.buf + ((size_t)b * (a.S + a.T) + a.S + len % a.T) * a.R);
-        for (int c = threadIdx.x; c < (a.R >> 4); c += blockDim.x) dst[c] = src[c];
+        // Sliding tail: the slot still holds token len - T, which leaves the
+        // tail now; its row goes back to its host row first (zero-copy
+        // stores into the mapped pool), chunk by chunk before the overwrite.
+        uint4* back = (a.sliding && len >= a.T)
+            ? reinterpret_cast<uint4*>(a.pool + ((size_t)b * a.H + (size_t)(len - a.T)) * a.R)
+            : nullptr;
+        for (int c = threadIdx.x; c < (a.R >> 4); c += blockDim.x) {
+            if (back) back[c] = dst[c];
+            dst[c] = src[c];
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {

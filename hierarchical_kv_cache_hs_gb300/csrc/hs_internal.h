@@ -40,6 +40,9 @@ struct ResolveArgs {
     int rows_per_group;
     unsigned* done;        // CTAs finished this call (returns to 0 after each call)
     int fifo;              // 1: FIFO eviction (hits keep their fill stamp), 0: LRU
+    int sliding;           // 1: the tail is [len - T, len) per request; 0: [C - T, C)
+    int alias;             // 1: a repeated token takes its first occurrence's slot (several
+                           //    draft positions in one row); 0: a repeat is an error
 };
 
 struct CopyArgs {
@@ -62,6 +65,9 @@ struct AppendArgs {
     int32_t* len;
     HsDevState* st;
     int S, T, R, C, cold;
+    uint8_t* pool;         // sliding tail: device-usable address of the mapped host pool
+    long long H;
+    int sliding;
 };
 
 // Launch geometry and shared-memory layout of the resolve kernel.

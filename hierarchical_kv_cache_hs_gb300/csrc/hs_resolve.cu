@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int step = a.st->step + 1;
     const int len = a.len[b];
+    // First tail position: fixed at C - T, or sliding with the request's length.
+    const int cold = a.sliding ? (len - a.T > 0 ? len - a.T : 0) : a.cold;
     const int32_t* g_topk = a.topk + (size_t)b * K;
     int32_t* g_out = a.out + (size_t)b * K;
     int32_t* g_stamp = a.stamp + (size_t)b * S;
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 err |= HS_E_RANGE;
             } else {
                 cl[e] = C_MISS;  // valid; refined below
-                if (t < a.cold) sl[e] = g_tok_slot[t];
+                if (t < cold) sl[e] = g_tok_slot[t];
             }
         }
     }
@@ -260,8 +262,12 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 // stamp; both differ from its own claim step + K - j.
                 if (s_stamp[sl[e]] != step + (K - j)) {
                     cl[e] = C_BAD;
-                    err |= HS_E_DUP;
-                    g_out[j] = -1;
+                    if (a.alias) {
+                        g_out[j] = sl[e];  // the same resident slot as its first occurrence
+                    } else {
+                        err |= HS_E_DUP;
+                        g_out[j] = -1;
+                    }
                 } else {
                     cl[e] = C_HIT;
                     // LRU: a hit refreshes its entry.  FIFO: the slot only
@@ -274,9 +280,17 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 }
             } else if (s_hj[hs[e]] != j) {
                 cl[e] = C_BAD;
-                err |= HS_E_DUP;
-                g_out[j] = -1;
-            } else if (tk[e] >= a.cold) {
+                if (!a.alias) {
+                    err |= HS_E_DUP;
+                    g_out[j] = -1;
+                } else if (tk[e] >= cold) {
+                    g_out[j] = S + tk[e] % a.T;
+                } else {
+                    // A repeated miss: its slot is known only after the
+                    // pairing.  Leave -(first + 2) and resolve it at the end.
+                    g_out[j] = -(s_hj[hs[e]] + 2);
+                }
+            } else if (tk[e] >= cold) {
                 cl[e] = C_TAIL;
                 g_out[j] = S + tk[e] % a.T;
                 ++ni;
@@ -498,6 +512,17 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
         }
     }
     __syncthreads();
+    if (a.alias && m > 0) {
+        // Repeated misses take the slot their first occurrence was paired with
+        // (written to out_slot above, before the barrier).
+        for (int e = 0; e < EMAX; ++e) {
+            const int j = j0 + e;
+            if (e < E && j < K) {
+                const int o = g_out[j];
+                if (o <= -2) g_out[j] = g_out[-o - 2];
+            }
+        }
+    }
     if (a.fifo) {
         for (int i = tid; i < S; i += NT)
             if (!((s_hitbits[i >> 5] >> (i & 31)) & 1u)) g_stamp[i] = s_stamp[i];

@@ -31,6 +31,9 @@ HS_E_RANGE = 1
 HS_E_DUP = 2
 HS_E_APPEND = 4
 
+HS_TAIL_FIXED = 0
+HS_TAIL_SLIDING = 1
+
 HS_POLICY_LRU = 0
 HS_POLICY_FIFO = 1
 
@@ -74,6 +77,7 @@ def _load():
         "hs_destroy": ([P], None),
         "hs_resolve": ([P, P, I, P, P], I),
         "hs_resolve_host": ([P, P, I, P, P], I),
+        "hs_resolve_multi": ([P, P, I, I, P, P], I),
         "hs_resolve_ce": ([P, P, I, P, P], I),
         "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
         "hs_host_pool": ([P], P),
@@ -92,6 +96,7 @@ def _load():
         "hs_set_copy_mode": ([P, I], I),
         "hs_resolve_launches": ([P], I),
         "hs_set_policy": ([P, I], I),
+        "hs_set_tail_mode": ([P, I], I),
         "hs_resolve_noalloc": ([I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], I),
         "hs_error_string": ([I], ctypes.c_char_p),
     }
@@ -164,6 +169,12 @@ def hs_resolve(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
 
 def hs_resolve_rc(h: int, topk_idx, K: int, out_slot, stream=None) -> int:
     return lib.hs_resolve(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream))
+
+
+def hs_resolve_multi(h: int, topk_idx, P: int, K: int, out_slot, stream=None) -> None:
+    """P draft positions' top-k rows ([B][P][K]) resolved together."""
+    _check(lib.hs_resolve_multi(h, _ptr(topk_idx), int(P), int(K), _ptr(out_slot),
+                                _stream(stream)), "hs_resolve_multi")
 
 
 def hs_resolve_host(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
@@ -272,6 +283,10 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
 
 def hs_set_copy_mode(h: int, mode: int) -> None:
     _check(lib.hs_set_copy_mode(h, int(mode)), "hs_set_copy_mode")
+
+
+def hs_set_tail_mode(h: int, mode: int) -> None:
+    _check(lib.hs_set_tail_mode(h, int(mode)), "hs_set_tail_mode")
 
 
 def hs_set_policy(h: int, policy: int) -> None:

@@ -118,6 +118,7 @@ class Workload:
     zipf_a: float = 1.1
     row_bytes: int = 1152
     seed: int = 0
+    sliding: bool = False   # the tail holds the last T tokens written (else [C - T, C))
 
     @property
     def H(self) -> int:

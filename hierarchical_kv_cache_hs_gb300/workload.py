@@ -42,7 +42,14 @@ class GpuWorkload:
             hs.hs_set_copy_mode(h.h, copy_mode)
             # Cold rows of request b live at pool row t of request slot b.
             self._fill_pool(h, layer, reqs, threads)
-            if wl.grow:
+            if wl.sliding:
+                # The tail holds the last T tokens written.
+                hs.hs_set_tail_mode(h.h, hs.HS_TAIL_SLIDING)
+                hs.hs_set_lengths(h.h, np.full(B, wl.len0, dtype=np.int32))
+                first = max(wl.len0 - wl.T, 0)
+                for i, b in enumerate(reqs):
+                    hs.hs_set_tail_rows(h.h, i, first, tg.rows(wl, layer, b, first, wl.len0 - first))
+            elif wl.grow:
                 hs.hs_set_lengths(h.h, np.full(B, wl.len0, dtype=np.int32))
             elif wl.T > 0:
                 for i, b in enumerate(reqs):
@@ -117,11 +124,16 @@ class GpuWorkload:
             hs.hs_resolve_host(h.h, self.topk_host[layer, s], wl.K, out_host[layer], stream)
 
     def reset(self) -> None:
+        """Back to the start state (a sliding tail's written-back host rows stay)."""
         wl = self.wl
-        for h in self.handles:
+        for layer, h in enumerate(self.handles):
             hs.hs_reset(h.h)
-            if wl.grow:
+            if wl.grow or wl.sliding:
                 hs.hs_set_lengths(h.h, np.full(wl.B, wl.len0, dtype=np.int32))
+            if wl.sliding:
+                first = max(wl.len0 - wl.T, 0)
+                for i, b in enumerate(self.requests):
+                    hs.hs_set_tail_rows(h.h, i, first, tg.rows(wl, layer, b, first, wl.len0 - first))
 
     def close(self) -> None:
         for h in self.handles:

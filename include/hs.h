@@ -127,6 +127,19 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                hs_stream_t stream);
 
 /*
+ * Several draft positions in one step (speculative decoding; vLLM Hybrid
+ * HiSparse post, "Speculative Decoding": a per-step resolver plan over the
+ * request's shared hot state).  topk_idx (device, [B][P][K]) holds P top-k
+ * rows per request; they are resolved as one row of P*K entries, and a
+ * repeated token -- across positions or within one -- is not an error: it
+ * gets the slot of its first occurrence and is fetched and counted once.
+ * out_slot is [B][P][K].  1 <= P*K <= min(S, HS_MAX_TOPK).  A retried step
+ * is simply another call.  Asynchronous; graph-capturable.
+ */
+int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_t* out_slot,
+                     hs_stream_t stream);
+
+/*
  * The same step from host memory: copies topk_idx (host, [B][K]) to the
  * device, resolves, copies out_slot (host, [B][K]) back and synchronises the
  * stream before returning.  Pinned host buffers give the fastest copies.
@@ -172,8 +185,10 @@ int hs_set_lengths(hs_handle* h, const int32_t* len_host);
 /*
  * Mixed residency, growing context: for every request b write row b of
  * rows_dev (device, [B][R]) as token len[b] into tail slot S + (len[b] mod T)
- * and advance len[b].  A request whose next token is outside the tail
- * ([C - T, C)) is left unchanged and HS_E_APPEND is latched.  Asynchronous;
+ * and advance len[b].  With a fixed tail, a request whose next token is
+ * outside [C - T, C) is left unchanged and HS_E_APPEND is latched; with a
+ * sliding tail (hs_set_tail_mode) only len[b] = C is refused, and the token
+ * leaving the tail is first written back to the host pool.  Asynchronous;
  * graph-capturable.  Requires T > 0.
  */
 int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream);
@@ -251,6 +266,23 @@ int hs_set_copy_mode(hs_handle* h, int mode);
 #define HS_POLICY_LRU   0
 #define HS_POLICY_FIFO  1
 int hs_set_policy(hs_handle* h, int policy);
+
+/*
+ * Which tokens the resident tail holds (vLLM Hybrid HiSparse post, "Mixed
+ * Residency": the tail stays on the GPU, older pages move to host memory):
+ *   HS_TAIL_FIXED    the last T positions of the capacity, [C - T, C)
+ *                    (default; hs_append fills it until len reaches C);
+ *   HS_TAIL_SLIDING  the last T tokens written, [len - T, len) per request.
+ *                    hs_append first writes the row of the token leaving the
+ *                    tail (position len - T) back to its host-pool row, so it
+ *                    is from then on an ordinary host-backed token (the post's
+ *                    "Full Residency" pre-copy).  hs_set_tail_rows then takes
+ *                    any token below C: write the current last T tokens.
+ * Setup only (before the first hs_resolve); sliding needs resident_tail > 0.
+ */
+#define HS_TAIL_FIXED    0
+#define HS_TAIL_SLIDING  1
+int hs_set_tail_mode(hs_handle* h, int mode);
 
 /* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG. */
 int hs_resolve_launches(hs_handle* h);

@@ -215,6 +215,58 @@ def test_parity_copy_engine_variant(name):
         res.workload.close()
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["fused", "split"])
+def test_parity_multi_position(mode):
+    """Two draft positions per step: the second row repeats about half of the
+    first's tokens; repeats share their first occurrence's slot."""
+    import oracle
+    from hierarchical_kv_cache_hs_gb300 import hs
+    P, Kp, B, C, S, R = 2, 512, 24, 16384, 2048, 1152
+    wl = tg.Workload("multi", 88, B=B, C=C, K=Kp, S=S, T=0, host_ratio=8, layers=2, steps=40,
+                     len0=C, grow=0, carry_pct=70, zipf_pct=30, third=tg.THIRD_ZIPF)
+    t0 = tg.topk_trace(wl, layer=0)
+    t1 = tg.topk_trace(wl, layer=1)
+    rng = np.random.default_rng(3)
+    take = rng.random(t1.shape) < 0.5
+    pick = rng.integers(0, Kp, size=t1.shape)
+    t1 = np.where(take, np.take_along_axis(t0, pick, axis=2), t1)
+    trace = np.ascontiguousarray(np.concatenate([t0, t1], axis=2))  # [steps][B][P*K]
+    h = hs.Handle(B, C, R, S, 8, 0)
+    try:
+        hs.hs_set_copy_mode(h.h, mode)
+        pool = h.host_pool()
+        for b in range(B):
+            pool[b, :C] = tg.rows(wl, 0, b, 0, C)
+        dev = torch.from_numpy(trace).cuda()
+        out = torch.empty_like(dev)
+        for s in range(wl.steps):
+            hs.hs_resolve_multi(h.h, dev[s], P, Kp, out[s])
+        torch.cuda.synchronize()
+        out = out.cpu().numpy()
+        tok, slot_tok, stamp, step = h.export_state()
+        stats = h.stats()
+        tot_m = 0
+        for b in range(B):
+            st = oracle.RequestState(C, S, 0, R)
+            host = pool[b, :C].copy()
+            for s in range(wl.steps):
+                o, c, e = st.resolve(host, trace[s, b], s + 1, alias=True)
+                np.testing.assert_array_equal(out[s, b], o, err_msg="step %d request %d" % (s, b))
+                assert e == 0
+                tot_m += c[1]
+            np.testing.assert_array_equal(tok[b], st.tok_slot)
+            np.testing.assert_array_equal(slot_tok[b], st.slot_tok)
+            np.testing.assert_array_equal(stamp[b], st.stamp)
+            buf = h.export_buffer(b)
+            occ = np.nonzero(st.slot_tok >= 0)[0]
+            np.testing.assert_array_equal(buf[occ], st.buf[occ])
+        assert stats["misses"] == tot_m and stats["err_bits"] == 0
+        # repeats really occurred, across and within positions
+        assert (out[:, :, Kp:][take] >= 0).all()
+    finally:
+        h.close()
+
+
 def test_resolve_host_matches_device_path():
     from hierarchical_kv_cache_hs_gb300 import hs
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
