@@ -456,6 +456,8 @@ def run_ours(args, rank, world, dist):
         "clocks": clocks,
         "wall_s_timed_region": main["wall_s"],
     }
+    if args.overlap and rank == 0:
+        line["layer_overlap"] = layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev)
     if "ce_s" in main:
         ce_value = wl.B * wl.layers * main["ce_steps"] / main["ce_s"]
         line["copy_engine_variant"] = {
@@ -471,6 +473,40 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args, total_steps)
     return line
+
+
+def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
+    """Independent layers on one stream vs one stream per layer."""
+    wl = tg.WORKLOADS["b64_c128k_l4_tail4096"]
+    steps = PRIME_STEPS + args.warmup + args.steps
+    w = GpuWorkload(wl, steps=steps)
+    out = {"workload": _workload_desc(wl)}
+    try:
+        main = torch.cuda.Stream(device=dev)
+        lstreams = [torch.cuda.Stream(device=dev) for _ in range(wl.layers)]
+        for name, ls in (("one_stream", None), ("stream_per_layer", lstreams)):
+            w.reset()
+            ms = 0.0
+            with torch.cuda.stream(main):
+                for s in range(PRIME_STEPS + args.warmup):
+                    w.launch_step(s, main, layer_streams=ls)
+                for i in range(args.steps):
+                    s = PRIME_STEPS + args.warmup + i
+                    flush.fill_(i & 0xFF)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(main)
+                    w.launch_step(s, main, layer_streams=ls)
+                    e1.record(main)
+                    e1.synchronize()
+                    ms += e0.elapsed_time(e1)
+            out[name] = {"resolves_per_s": wl.B * wl.layers * args.steps / (ms / 1e3),
+                         "ms_per_step": ms / args.steps}
+        misses = sum(hs.hs_stats(h.h)["misses"] for h in w.handles)
+        out["misses_last_pass"] = misses
+    finally:
+        w.close()
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -560,6 +596,9 @@ def main():
                     help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass")
     ap.add_argument("--no-ce", action="store_true", help="skip the copy-engine comparison variant")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time the 4-layer, 128K-context workload with its layers on one "
+                         "stream and on one stream per layer")
     ap.add_argument("--copy-mode", choices=["auto", "fused", "split"], default="auto",
                     help="launch mode of the step (identical results; see hs_set_copy_mode)")
     args = ap.parse_args()

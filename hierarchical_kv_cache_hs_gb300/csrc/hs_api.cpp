@@ -550,6 +550,18 @@ int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_s
     if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
     DeviceGuard g(h->device);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Pinned, mapped host buffers: the kernels read the top-k rows and write
+    // out_slot across the host link themselves -- no staging copies.
+    void* d_in = nullptr;
+    void* d_out = nullptr;
+    if (cudaHostGetDevicePointer(&d_in, const_cast<int32_t*>(topk_idx), 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&d_out, out_slot, 0) == cudaSuccess) {
+        const int rc = hs_resolve(h, static_cast<const int32_t*>(d_in), K,
+                                  static_cast<int32_t*>(d_out), stream);
+        if (rc != HS_OK) return rc;
+        return cudaStreamSynchronize(s) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+    }
+    cudaGetLastError();  // not mapped: clear the lookup's error and stage through the device
     const size_t bytes = (size_t)h->B * (size_t)K * sizeof(int32_t);
     if (cudaMemcpyAsync(h->d_stage_in, topk_idx, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return HS_ERR_CUDA;

@@ -96,12 +96,33 @@ class GpuWorkload:
     def out_at(self, layer: int, step: int) -> torch.Tensor:
         return self.out[layer, step] if self.record else self.out[layer]
 
-    def launch_step(self, s: int, stream=None, copy_engine: bool = False) -> int:
+    def launch_step(self, s: int, stream=None, copy_engine: bool = False,
+                    layer_streams=None) -> int:
         """Enqueue step s for every layer; returns the number of kernel launches.
 
         ``copy_engine`` uses the copy-engine comparison variant (hs_resolve_ce),
-        which synchronises the stream inside every call."""
+        which synchronises the stream inside every call.  ``layer_streams``
+        (one torch stream per layer) runs the independent layers concurrently:
+        each waits for ``stream`` at the start and ``stream`` waits for all of
+        them at the end, so one layer's resolve overlaps another's row fetch."""
         wl = self.wl
+        if layer_streams is not None:
+            main = stream if stream is not None else torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            fork.record(main)
+            n = 0
+            for layer, h in enumerate(self.handles):
+                ls = layer_streams[layer]
+                ls.wait_event(fork)
+                if self.append_rows is not None:
+                    hs.hs_append(h.h, self.append_rows[layer, s], ls)
+                    n += 1
+                hs.hs_resolve(h.h, self.topk[layer, s], wl.K, self.out_at(layer, s), ls)
+                n += hs.hs_resolve_launches(h.h)
+                join = torch.cuda.Event()
+                join.record(ls)
+                main.wait_event(join)
+            return n
         n = 0
         for layer, h in enumerate(self.handles):
             if self.append_rows is not None:

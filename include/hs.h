@@ -140,10 +140,13 @@ int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_
                      hs_stream_t stream);
 
 /*
- * The same step from host memory: copies topk_idx (host, [B][K]) to the
- * device, resolves, copies out_slot (host, [B][K]) back and synchronises the
- * stream before returning.  Pinned host buffers give the fastest copies.
- * Not graph-capturable (it synchronises).
+ * The same step from host memory: topk_idx (host, [B][K]) in, out_slot (host,
+ * [B][K]) out; synchronises the stream before returning.  When both buffers
+ * are page-locked and mapped into the device address space (cudaHostAlloc,
+ * cudaMallocHost, or cudaHostRegister with mapping), the kernels read and
+ * write them across the host link directly; otherwise they are staged
+ * through device buffers with two cudaMemcpyAsync.  Not graph-capturable
+ * (it synchronises).
  */
 int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                     hs_stream_t stream);

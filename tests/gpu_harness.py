@@ -22,7 +22,7 @@ class GpuResult:
 
 
 def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO,
-            policy=hs.HS_POLICY_LRU, copy_engine=False):
+            policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False):
     """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one."""
     w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
     for h in w.handles:
@@ -36,6 +36,7 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
     res = GpuResult()
     res.misses = np.zeros((wl.layers, steps, wl.B), dtype=np.int32)
     stream = torch.cuda.Stream()
+    lstreams = [torch.cuda.Stream() for _ in range(wl.layers)] if layer_streams else None
     if graph:
         # Warm the kernels up outside the capture, then restart from the empty state.
         with torch.cuda.stream(stream):
@@ -45,14 +46,14 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for s in range(steps):
-                w.launch_step(s, torch.cuda.current_stream())
+                w.launch_step(s, torch.cuda.current_stream(), layer_streams=lstreams)
         g.replay()
         torch.cuda.synchronize()
         res.misses = None  # per-step counts are not observable inside one graph
     else:
         with torch.cuda.stream(stream):
             for s in range(steps):
-                w.launch_step(s, stream, copy_engine=copy_engine)
+                w.launch_step(s, stream, copy_engine=copy_engine, layer_streams=lstreams)
                 for layer, h in enumerate(w.handles):
                     hs.hs_stats(h.h, res.misses[layer, s])
     torch.cuda.synchronize()

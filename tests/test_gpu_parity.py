@@ -71,6 +71,18 @@ def test_parity_b64_four_layers_tail4096():
     _run_and_compare(wl)
 
 
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_parity_layers_on_concurrent_streams(graph):
+    """The four independent layers on one stream each (fork/join events)."""
+    from gpu_harness import check_counters, compare, gpu_run
+    wl = tg.WORKLOADS["b64_c128k_l4_tail4096"]
+    res = gpu_run(wl, steps=40, graph=graph, layer_streams=True)
+    try:
+        tot, err = compare(wl, res, requests=[0, 21, 63])
+    finally:
+        res.workload.close()
+
+
 EDGE = {
     # ragged: K and S not multiples of the CTA width, B odd
     "ragged": tg.Workload("ragged", 91, B=3, C=5000, K=1000, S=3000, T=0, host_ratio=2, layers=1,
@@ -285,6 +297,17 @@ def test_resolve_host_matches_device_path():
         for x, y in zip(ta[:3], tb[:3]):
             np.testing.assert_array_equal(x, y)
         assert hs.hs_stats(a.handles[0].h) == hs.hs_stats(b.handles[0].h)
+        # pageable (unmapped) host buffers take the staged path
+        c = GpuWorkload(wl, steps=steps, record=False)
+        try:
+            pageable_in = c.topk.cpu().numpy()
+            pageable_out = np.empty((wl.B, wl.K), dtype=np.int32)
+            for s in range(steps):
+                hs.hs_resolve_host(c.handles[0].h, np.ascontiguousarray(pageable_in[0, s]), wl.K,
+                                   pageable_out)
+                assert (a.out[0, s].cpu().numpy() == pageable_out).all()
+        finally:
+            c.close()
     finally:
         a.close()
         b.close()
