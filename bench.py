@@ -36,6 +36,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 PRIME_STEPS = 10
+# DRAM (read + write) and host-link read bytes of one steady-state launch of the
+# fused swap-in kernel on the 64-request, 64K-context, 4096-slot workload, from
+# its ncu capture (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md).  The
+# host-link bytes equal the algorithmic miss-row bytes of that launch.
+FUSED_NCU_DRAM_BYTES = 9063424 + 846336
+FUSED_NCU_SYSMEM_BYTES = 933264 * 32
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -439,7 +445,11 @@ def run_ours(args, rank, world, dist):
                      "kernel": "hs_resolve_kernel<fused> (resolve + row fetch)" if fused else "hs_copy_kernel",
                      "achieved": copy_gbs,
                      "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
-                     "traffic": None,
+                     # ncu, one steady-state launch of this kernel on this workload
+                     # (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md); None when
+                     # another kernel or workload is timed
+                     "traffic": FUSED_NCU_DRAM_BYTES if (fused and wl.name == "b64_c64k_s4096") else None,
+                     "traffic_host_link": FUSED_NCU_SYSMEM_BYTES if (fused and wl.name == "b64_c64k_s4096") else None,
                      "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
                                     "1 GiB zero-copy 128-bit read kernel)"},
         "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if fused else
