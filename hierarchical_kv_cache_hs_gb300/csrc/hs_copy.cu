@@ -5,7 +5,8 @@
 //
 // The rows of all requests are flattened into one list (prefix sum of the
 // per-request miss counts, computed by every CTA in shared memory) so that no
-// SM idles on a request with few misses.  A warp copies `rows_per_group`
+// SM idles on a request with few misses; each warp takes an equal contiguous
+// run of it.  A warp copies `rows_per_group`
 // rows at a time: its first lanes look up one row each (request, token,
 // victim slot), then every lane streams 16-byte chunks of those rows with
 // zero-copy loads from the mapped host pool -- U independent loads in flight
@@ -81,10 +82,17 @@ __global__ void __launch_bounds__(CT) hs_copy_kernel(CopyArgs a)
     const int gw = (int)((blockIdx.x * (unsigned)CT + tid) >> 5);
     const int nw = (int)((gridDim.x * (unsigned)CT) >> 5);
 
-    for (long long r0 = (long long)gw * G; r0 < total; r0 += (long long)nw * G) {
+    // Each warp copies one contiguous run of the flattened list, so it reads
+    // the rows of one or two requests: a narrow window of the host pool per
+    // SM.  (Striding the groups over the whole grid scattered every SM's reads
+    // over the whole pool, and cost a third of the rate on 38 GB of pools.)
+    const long long per = ((total + nw - 1) / nw + G - 1) / G * G;
+    const long long beg = (long long)gw * per;
+    const long long end = beg + per < total ? beg + per : total;
+    for (long long r0 = beg; r0 < end; r0 += G) {
         long long src = 0, dst = 0;
         const long long r = r0 + lane;
-        if (lane < G && r < total) {
+        if (lane < G && r < end) {
             int lo = 0, hi = a.B - 1;  // request b with s_pref[b] <= r < s_pref[b + 1]
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(CT) hs_copy_kernel(CopyArgs a)
             src = a.flat_src ? r * a.R : ((long long)lo * a.H + a.miss_tok[li]) * a.R;
             dst = ((long long)lo * slots + a.miss_slot[li]) * a.R;
         }
-        const int nrows = (int)((total - r0) < G ? (total - r0) : G);
+        const int nrows = (int)((end - r0) < G ? (end - r0) : G);
         const int nch = nrows * cpr;
         for (int c0 = 0; c0 < nch; c0 += 32 * U) {
             uint4 v[U];

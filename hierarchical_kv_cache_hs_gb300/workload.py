@@ -137,12 +137,19 @@ class GpuWorkload:
         return n
 
     def host_step(self, s: int, out_host: torch.Tensor, stream=None) -> None:
-        """Step s from host buffers (hs_resolve_host), for end-to-end timing."""
+        """Step s from host buffers (hs_resolve_host), for end-to-end timing.
+
+        The top-k rows and results are passed as raw addresses into the pinned
+        [layers][steps][B][K] trace and the [layers][B][K] output."""
         wl = self.wl
+        row = wl.B * wl.K * 4
+        base_in = self.topk_host.data_ptr()
+        base_out = out_host.data_ptr()
         for layer, h in enumerate(self.handles):
             if self.append_rows is not None:
                 hs.hs_append(h.h, self.append_rows[layer, s], stream)
-            hs.hs_resolve_host(h.h, self.topk_host[layer, s], wl.K, out_host[layer], stream)
+            hs.hs_resolve_host(h.h, base_in + (layer * self.steps + s) * row, wl.K,
+                               base_out + layer * row, stream)
 
     def reset(self) -> None:
         """Back to the start state (a sliding tail's written-back host rows stay)."""
