@@ -40,7 +40,7 @@ PRIME_STEPS = 10
 # fused swap-in kernel on the 64-request, 64K-context, 4096-slot workload, from
 # its ncu capture (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md).  The
 # host-link bytes equal the algorithmic miss-row bytes of that launch.
-FUSED_NCU_DRAM_BYTES = 9063424 + 846336
+FUSED_NCU_DRAM_BYTES = 9065472 + 886272
 FUSED_NCU_SYSMEM_BYTES = 933264 * 32
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20

@@ -136,6 +136,12 @@ __device__ __forceinline__ void copy_row_group(const uint8_t* pool_b, uint8_t* b
     }
 }
 
+// A stamp clamped into [0, step - 1], the range the victim search assumes.
+__device__ __forceinline__ int clamp_stamp(int k, int step)
+{
+    return k < 0 ? 0 : (k >= step ? step - 1 : k);
+}
+
 template <bool FUSED, int U>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
 {
@@ -165,7 +171,16 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int step = a.st->step + 1;
+    // State the caller owns (the allocation-free entry point) may be
+    // inconsistent; each repair below latches HS_E_STATE.  The step counter
+    // must leave room for the claims step + K - j to stay below 2^31.
+    int bad_state = 0;
+    int step0 = a.st->step;
+    if (step0 < 0 || step0 >= HS_MAX_STEP) {
+        step0 = step0 < 0 ? 0 : HS_MAX_STEP - 1;
+        bad_state = HS_E_STATE;
+    }
+    const int step = step0 + 1;
     const int len = a.len[b];
     // First tail position: fixed at C - T, or sliding with the request's length.
     const int cold = a.sliding ? (len - a.T > 0 ? len - a.T : 0) : a.cold;
@@ -207,12 +222,36 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     if (a.fifo)
         for (int i = tid; i < ((S + 31) >> 5); i += NT) s_hitbits[i] = 0u;
     if (vec_rows) cp_async_wait_all();
+    // Every stamp must lie in [0, step - 1] for the victim search to place
+    // exactly m victims: each thread clamps the stamps it loaded itself (as
+    // 16-byte words when it copied them so, which keeps the reads free of
+    // bank conflicts).
+    if (vec_rows) {
+        int4* s4 = reinterpret_cast<int4*>(s_stamp);
+        for (int i = tid; i < (S >> 2); i += NT) {
+            const int4 k = s4[i];
+            if ((unsigned)k.x >= (unsigned)step || (unsigned)k.y >= (unsigned)step ||
+                (unsigned)k.z >= (unsigned)step || (unsigned)k.w >= (unsigned)step) {
+                s4[i] = make_int4(clamp_stamp(k.x, step), clamp_stamp(k.y, step),
+                                  clamp_stamp(k.z, step), clamp_stamp(k.w, step));
+                bad_state = HS_E_STATE;
+            }
+        }
+    } else {
+        for (int i = tid; i < S; i += NT) {
+            const int k = s_stamp[i];
+            if ((unsigned)k >= (unsigned)step) {
+                s_stamp[i] = clamp_stamp(k, step);
+                bad_state = HS_E_STATE;
+            }
+        }
+    }
     if (tid < 3) s_cnt[tid] = 0;
     __syncthreads();
 
     // ---- (1) classify, gather the page table, find repeats ----------------
     int cl[EMAX], hs[EMAX], sl[EMAX];
-    int err = 0;
+    int err = bad_state;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         const int t = tk[e];
@@ -235,6 +274,11 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     // valid token (a miss or a tail token) goes through the hash.
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
+        // A page-table entry outside [-1, S) is corrupt state: resolve as a miss.
+        if (sl[e] < -1 || sl[e] >= S) {
+            sl[e] = -1;
+            err |= HS_E_STATE;
+        }
         if (cl[e] == C_MISS && sl[e] >= 0) atomicMax(&s_stamp[sl[e]], step + (K - (j0 + e)));
     }
 #pragma unroll
@@ -500,7 +544,10 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                 const int t = s_mtok[i];
                 const int v = s_vic[i];
                 const int old = s_slot_tok[v];
-                if (old >= 0) g_tok_slot[old] = -1;  // the evicted token leaves the table
+                // the evicted token leaves the table (an entry outside
+                // [-1, C) is corrupt state and is not written through)
+                if (old >= 0 && old < a.C) g_tok_slot[old] = -1;
+                else if (old != -1) atomicOr(&s_cnt[2], HS_E_STATE);
                 g_slot_tok[v] = t;
                 g_tok_slot[t] = v;
                 s_stamp[v] = step;
@@ -521,7 +568,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
                     const int t = s_mtok[i];
                     const int v = s_vic[i];
                     const int old = s_slot_tok[v];
-                    if (old >= 0) g_tok_slot[old] = -1;
+                    if (old >= 0 && old < a.C) g_tok_slot[old] = -1;
+                    else if (old != -1) atomicOr(&s_cnt[2], HS_E_STATE);
                     g_slot_tok[v] = t;
                     g_tok_slot[t] = v;
                     s_stamp[v] = step;

@@ -30,6 +30,7 @@ HS_ERR_LIMIT = -6
 HS_E_RANGE = 1
 HS_E_DUP = 2
 HS_E_APPEND = 4
+HS_E_STATE = 8
 
 HS_TAIL_FIXED = 0
 HS_TAIL_SLIDING = 1

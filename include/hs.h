@@ -77,6 +77,14 @@ typedef struct CUstream_st* hs_stream_t;
 #define HS_E_RANGE   1  /* an index < -1 or >= the request's current length */
 #define HS_E_DUP     2  /* an index repeated within one top-k row */
 #define HS_E_APPEND  4  /* hs_append with no room in the resident tail */
+#define HS_E_STATE   8  /* inconsistent state met and repaired for this step
+                           (caller-owned tables of hs_resolve_noalloc, or a step
+                           counter run past HS_MAX_STEP): a step counter outside
+                           [0, HS_MAX_STEP) or a stamp outside [0, step - 1] was
+                           clamped, a token->slot entry outside [-1, S) was taken
+                           as a miss, or a slot->token entry outside [-1, C) was
+                           not written through.  Results stay in range; LRU
+                           order among the repaired entries is unspecified. */
 
 /* Kernel limits.  The step counter runs up to HS_MAX_STEP (stamps and the
  * in-kernel claim of a slot, step + K, stay below 2^31). */

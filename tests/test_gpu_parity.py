@@ -279,6 +279,55 @@ def test_parity_multi_position(mode):
         h.close()
 
 
+@pytest.mark.parametrize("step0", [100, 1 << 21, -5, 0x7FFFFFF0])
+def test_corrupt_caller_state_is_contained(step0):
+    """Tables a caller owns (hs_resolve_noalloc) may be garbage: out-of-range
+    page-table and slot entries and stamps beyond the step counter.  The step
+    must stay inside its buffers, return slots in range and latch HS_E_STATE;
+    the context stays usable afterwards."""
+    from hierarchical_kv_cache_hs_gb300 import hs
+    B, C, S, K, R, ratio = 4, 4096, 512, 256, 64, 8
+    rng = np.random.default_rng(11)
+    h = hs.Handle(B, C, R, S, ratio, 0)  # only for its pinned host pool
+    try:
+        dev = "cuda"
+        tok = rng.integers(-1, S, size=(B, C)).astype(np.int32)
+        bad = rng.random((B, C)) < 0.2
+        tok[bad] = rng.integers(S, 4 * S, size=bad.sum())
+        tok[rng.random((B, C)) < 0.05] = -7
+        slot_tok = rng.integers(-1, C, size=(B, S)).astype(np.int32)
+        slot_tok[rng.random((B, S)) < 0.2] = 10 * C
+        stamp = rng.integers(-50, 1 << 22, size=(B, S)).astype(np.int32)
+        t_tok = torch.from_numpy(tok).to(dev)
+        t_slot = torch.from_numpy(slot_tok).to(dev)
+        t_stamp = torch.from_numpy(stamp).to(dev)
+        lengths = torch.full((B,), C, dtype=torch.int32, device=dev)
+        buf = torch.zeros((B, S, R), dtype=torch.uint8, device=dev)
+        control = torch.zeros(8, dtype=torch.int32, device=dev)
+        control[0] = step0  # step counter, out of range in the last two cases
+        out = torch.empty((B, K), dtype=torch.int32, device=dev)
+        for s in range(3):
+            rows = np.stack([rng.choice(C, K, replace=False) for _ in range(B)]).astype(np.int32)
+            hs.hs_resolve_noalloc(B, C, R, S, h.H, 0, torch.from_numpy(rows).to(dev), K, out,
+                                  t_tok, t_slot, t_stamp, lengths, hs.hs_host_pool(h.h), buf,
+                                  control)
+            torch.cuda.synchronize()
+            o = out.cpu().numpy()
+            assert ((o == -1) | ((o >= 0) & (o < S))).all()
+        ctl = control.cpu().numpy()
+        assert ctl[0] == step0 + 3 and ctl[1] & hs.HS_E_STATE
+        # the context is still healthy
+        h2 = hs.Handle(2, 1024, 32, 64, 16)
+        try:
+            row = torch.arange(64, dtype=torch.int32, device=dev).repeat(2, 1).contiguous()
+            hs.hs_resolve(h2.h, row, 64, torch.empty_like(row))
+            assert h2.stats()["misses"] == 128 and h2.stats()["err_bits"] == 0
+        finally:
+            h2.close()
+    finally:
+        h.close()
+
+
 def test_resolve_host_matches_device_path():
     from hierarchical_kv_cache_hs_gb300 import hs
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
