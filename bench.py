@@ -215,6 +215,8 @@ def run_ours(args, rank, world, dist):
     mode = {"auto": hs.HS_COPY_AUTO, "fused": hs.HS_COPY_FUSED, "split": hs.HS_COPY_SPLIT}[args.copy_mode]
     fused = mode == hs.HS_COPY_FUSED or (mode == hs.HS_COPY_AUTO and wl.B >= hs.HS_FUSED_MIN_BATCH)
     total_steps = PRIME_STEPS + args.warmup + args.steps
+    # Several layers: one launch for all of them, or one call per layer.
+    one = args.layer_launch == "one" and wl.layers > 1
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -245,7 +247,7 @@ def run_ours(args, rank, world, dist):
             misses_per_step = []
             with torch.cuda.stream(stream):
                 for s in range(PRIME_STEPS + args.warmup):
-                    w.launch_step(s, stream)
+                    w.launch_step(s, stream, one_launch=one)
                 stream.synchronize()
                 m0 = stats_sum("misses")
                 barrier()
@@ -255,7 +257,7 @@ def run_ours(args, rank, world, dist):
                     s = PRIME_STEPS + args.warmup + i
                     flush.fill_(i & 0xFF)
                     starts[i].record(stream)
-                    launches += w.launch_step(s, stream)
+                    launches += w.launch_step(s, stream, one_launch=one)
                     ends[i].record(stream)
                 torch.cuda.synchronize()
                 barrier()
@@ -278,12 +280,25 @@ def run_ours(args, rank, world, dist):
                 last = np.zeros(wl.B, dtype=np.int32)
                 with torch.cuda.stream(stream):
                     for s in range(PRIME_STEPS + args.warmup):
-                        w.launch_step(s, stream)
+                        w.launch_step(s, stream, one_launch=one)
                     for i in range(args.steps):
                         s = PRIME_STEPS + args.warmup + i
                         flush.fill_(i & 0xFF)
                         tot = 0
                         cms = rms = 0.0
+                        if one:
+                            # One launch covers every layer: time it whole.
+                            before[i].record(stream)
+                            w.launch_step(s, stream, one_launch=True)
+                            after[i].record(stream)
+                            stream.synchronize()
+                            for h in w.handles:
+                                hs.hs_stats(h.h, last)
+                                tot += int(last.sum())
+                            misses_per_step.append(tot)
+                            copy_ms.append(before[i].elapsed_time(after[i]))
+                            resolve_ms.append(0.0)
+                            continue
                         for layer, h in enumerate(w.handles):
                             for e in (before[i], after[i], rs[i]):
                                 e.record(stream)
@@ -341,8 +356,7 @@ def run_ours(args, rank, world, dist):
             w.close()
         return res
 
-    sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(dev.index, args.clocks_csv)
     main = measure(wl, want_e2e=not args.no_e2e, want_ce=not args.no_ce)
     clocks = sampler.stop()
 
@@ -414,6 +428,7 @@ def run_ours(args, rank, world, dist):
     step_frac = t_roof / (main["dev_ms"] / 1e3)
 
     e2e_value = all_units / max_over_ranks(main["e2e_s"]) if "e2e_s" in main else None
+    launch_mode = "fused, all layers in one launch" if one else "fused" if fused else "split"
     line = {
         "metric": METRIC,
         "value": value,
@@ -432,7 +447,7 @@ def run_ours(args, rank, world, dist):
             "prime_steps_untimed": PRIME_STEPS,
             "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
             "parallelism": "requests sharded over ranks, no collective on the data path",
-            "launch_mode": "fused" if fused else "split",
+            "launch_mode": launch_mode,
         },
         "miss_row_gbs": miss_gbs,
         "h2d_peak": peaks,
@@ -442,7 +457,9 @@ def run_ours(args, rank, world, dist):
                           "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
                           "table_bytes_per_resolve": "16K + 4S + 16m"},
         "roofline": {"bound": "h2d",
-                     "kernel": "hs_resolve_kernel<fused> (resolve + row fetch)" if fused else "hs_copy_kernel",
+                     "kernel": ("hs_resolve_layers_kernel (every layer's resolve + row fetch, one grid)"
+                                if one else "hs_resolve_kernel<fused> (resolve + row fetch)"
+                                if fused else "hs_copy_kernel"),
                      "achieved": copy_gbs,
                      "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
                      # ncu, one steady-state launch of this kernel on this workload
@@ -452,10 +469,10 @@ def run_ours(args, rank, world, dist):
                      "traffic_host_link": FUSED_NCU_SYSMEM_BYTES if (fused and wl.name == "b64_c64k_s4096") else None,
                      "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
                                     "1 GiB zero-copy 128-bit read kernel)"},
-        "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if fused else
+        "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if (fused or one) else
                                {"copy": sum(main["copy_ms"]) / args.steps,
                                 "resolve": sum(main["resolve_ms"]) / args.steps}),
-        "launch_mode": "fused" if fused else "split",
+        "launch_mode": launch_mode,
         "misses_per_step_mean": statistics.mean(main["misses_per_step"]),
         "misses_per_step": main["misses_per_step"],
         "e2e": {"value": e2e_value, "unit": "resolves/s",
@@ -486,7 +503,8 @@ def run_ours(args, rank, world, dist):
 
 
 def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
-    """Independent layers on one stream vs one stream per layer."""
+    """Independent layers: one call per layer on one stream, one stream per layer,
+    or all layers in one launch."""
     wl = tg.WORKLOADS["b64_c128k_l4_tail4096"]
     steps = PRIME_STEPS + args.warmup + args.steps
     w = GpuWorkload(wl, steps=steps)
@@ -494,19 +512,20 @@ def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
     try:
         main = torch.cuda.Stream(device=dev)
         lstreams = [torch.cuda.Stream(device=dev) for _ in range(wl.layers)]
-        for name, ls in (("one_stream", None), ("stream_per_layer", lstreams)):
+        for name, ls, one in (("one_stream", None, False), ("stream_per_layer", lstreams, False),
+                              ("one_launch", None, True)):
             w.reset()
             ms = 0.0
             with torch.cuda.stream(main):
                 for s in range(PRIME_STEPS + args.warmup):
-                    w.launch_step(s, main, layer_streams=ls)
+                    w.launch_step(s, main, layer_streams=ls, one_launch=one)
                 for i in range(args.steps):
                     s = PRIME_STEPS + args.warmup + i
                     flush.fill_(i & 0xFF)
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(main)
-                    w.launch_step(s, main, layer_streams=ls)
+                    w.launch_step(s, main, layer_streams=ls, one_launch=one)
                     e1.record(main)
                     e1.synchronize()
                     ms += e0.elapsed_time(e1)
@@ -606,6 +625,10 @@ def main():
                     help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass")
     ap.add_argument("--no-ce", action="store_true", help="skip the copy-engine comparison variant")
+    ap.add_argument("--layer-launch", choices=["one", "loop"], default="one",
+                    help="several layers: all in one launch (hs_resolve_layers) or one call per layer")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the nvidia-smi clock samples of the timed region to this file")
     ap.add_argument("--overlap", action="store_true",
                     help="also time the 4-layer, 128K-context workload with its layers on one "
                          "stream and on one stream per layer")

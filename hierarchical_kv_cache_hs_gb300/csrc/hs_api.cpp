@@ -328,15 +328,10 @@ int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_
     return resolve_impl(h, topk_idx, (int)PK, out_slot, stream, 1);
 }
 
-static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
-                        hs_stream_t stream, int alias)
+// The resolve kernel's arguments for one handle's step.
+static ResolveArgs resolve_args(const hs_handle* h, const int32_t* topk_idx, int K,
+                                int32_t* out_slot, int alias)
 {
-    if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
-    if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
-    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
-    DeviceGuard g(h->device);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
     ResolveArgs ra;
     ra.topk = topk_idx;
     ra.out = out_slot;
@@ -364,6 +359,18 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
     ra.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
     ra.alias = alias;
+    return ra;
+}
+
+static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
+                        hs_stream_t stream, int alias)
+{
+    if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
+    if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const ResolveArgs ra = resolve_args(h, topk_idx, K, out_slot, alias);
 
     const bool prof = h->prof_before && h->prof_after;
     const bool fused = h->copy_mode == HS_COPY_FUSED ||
@@ -397,6 +404,44 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
     if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
     if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
+                      int32_t* const* out_slot, hs_stream_t stream)
+{
+    if (!handles || !topk_idx || !out_slot || L <= 0 || K <= 0) return HS_ERR_ARG;
+    if (L > HS_MAX_LAYERS) return HS_ERR_LIMIT;
+    const hs_handle* h0 = handles[0];
+    if (!valid(h0)) return HS_ERR_ARG;
+    for (int l = 0; l < L; ++l) {
+        const hs_handle* h = handles[l];
+        if (!valid(h) || !topk_idx[l] || !out_slot[l]) return HS_ERR_ARG;
+        if (h->B != h0->B || h->S != h0->S || h->R != h0->R || h->device != h0->device)
+            return HS_ERR_ARG;
+        for (int k = 0; k < l; ++k)
+            if (handles[k] == h) return HS_ERR_ARG;
+    }
+    if (K > h0->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h0->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    LayerArgs p;
+    p.B = h0->B;
+    for (int l = 0; l < L; ++l) p.l[l] = resolve_args(handles[l], topk_idx[l], K, out_slot[l], 0);
+    // Profiling events of any handle bracket the one launch.
+    for (int l = 0; l < L; ++l) {
+        const hs_handle* h = handles[l];
+        if (h->prof_before && h->prof_after && cudaEventRecord(h->prof_before, s) != cudaSuccess)
+            return HS_ERR_CUDA;
+    }
+    if (hs_launch_swapin_layers(p, L, h0->copy_unroll, s) != cudaSuccess) return HS_ERR_CUDA;
+    for (int l = 0; l < L; ++l) {
+        const hs_handle* h = handles[l];
+        if (h->prof_before && h->prof_after && cudaEventRecord(h->prof_after, s) != cudaSuccess)
+            return HS_ERR_CUDA;
+    }
     return HS_OK;
 }
 

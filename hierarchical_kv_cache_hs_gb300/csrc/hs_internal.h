@@ -45,6 +45,13 @@ struct ResolveArgs {
                            //    draft positions in one row); 0: a repeat is an error
 };
 
+// Several handles' steps in one launch (hs_resolve_layers): the first L
+// entries are used, all with the same K and S; each handle has B CTAs.
+struct LayerArgs {
+    ResolveArgs l[HS_MAX_LAYERS];
+    int B;
+};
+
 struct CopyArgs {
     const int32_t* miss_cnt;
     const int32_t* miss_tok;
@@ -104,6 +111,8 @@ cudaError_t hs_prepare_resolve();
 cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s);
 // Resolve + row fetch in one launch; advances the step counter itself.
 cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream_t s);
+// The same for L handles at once (L * B CTAs).
+cudaError_t hs_launch_swapin_layers(const LayerArgs& p, int L, int unroll, cudaStream_t s);
 
 // Copy kernel: `pdl` lets it launch while the resolve grid drains (it waits
 // on the resolve grid's completion before reading the miss lists).

@@ -142,8 +142,10 @@ __device__ __forceinline__ int clamp_stamp(int k, int step)
     return k < 0 ? 0 : (k >= step ? step - 1 : k);
 }
 
+// One request's step: CTA `b` of the `nblocks` that serve one handle.
 template <bool FUSED, int U>
-__global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
+__device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
+                                            const unsigned nblocks)
 {
     extern __shared__ __align__(16) int smem[];
     __shared__ int s_w[32];
@@ -169,7 +171,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
     uint16_t* s_vic = s_mj + K;                                 // [K]
     unsigned* s_hitbits = reinterpret_cast<unsigned*>(s_vic + K + (K & 1));  // [ceil(S/32)]
 
-    const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // State the caller owns (the allocation-free entry point) may be
     // inconsistent; each repair below latches HS_E_STATE.  The step counter
@@ -623,12 +624,28 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
             // to arrive advances it for the next call and re-arms the count.
             __threadfence();
             const unsigned prev = atomicAdd(a.done, 1u);
-            if (prev == gridDim.x - 1) {
+            if (prev == nblocks - 1) {
                 *a.done = 0u;
                 a.st->step = step;
             }
         }
     }
+}
+
+template <bool FUSED, int U>
+__global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
+{
+    resolve_cta<FUSED, U>(a, blockIdx.x, gridDim.x);
+}
+
+// Independent layers in one grid: CTA x serves request x mod B of layer
+// x / B.  The layers' CTAs then share the SMs, so while some resolve
+// others fetch rows, and one launch covers the whole step.
+template <int U>
+__global__ void __launch_bounds__(NT, 1) hs_resolve_layers_kernel(const __grid_constant__ LayerArgs p)
+{
+    const int layer = blockIdx.x / p.B;
+    resolve_cta<true, U>(p.l[layer], blockIdx.x - layer * p.B, (unsigned)p.B);
 }
 
 }  // namespace
@@ -656,6 +673,12 @@ cudaError_t hs_prepare_resolve()
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(hs_resolve_kernel<true, 8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_resolve_layers_kernel<9>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_resolve_layers_kernel<8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     return e;
 }
 
@@ -678,4 +701,15 @@ cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream
     cfg.stream = s;
     if (unroll == 9) return cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, 9>, a);
     return cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, 8>, a);
+}
+
+cudaError_t hs_launch_swapin_layers(const LayerArgs& p, int L, int unroll, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(L * p.B));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = hs_resolve_smem_bytes(p.l[0].K, p.l[0].S);
+    cfg.stream = s;
+    if (unroll == 9) return cudaLaunchKernelEx(&cfg, hs_resolve_layers_kernel<9>, p);
+    return cudaLaunchKernelEx(&cfg, hs_resolve_layers_kernel<8>, p);
 }

@@ -47,6 +47,7 @@ HS_MAX_TOPK = 4096
 HS_MAX_SLOTS = 16384
 HS_MAX_BATCH = 4096
 HS_MAX_ROW_BYTES = 65536
+HS_MAX_LAYERS = 16
 
 
 class HsError(RuntimeError):
@@ -79,6 +80,7 @@ def _load():
         "hs_resolve": ([P, P, I, P, P], I),
         "hs_resolve_host": ([P, P, I, P, P], I),
         "hs_resolve_multi": ([P, P, I, I, P, P], I),
+        "hs_resolve_layers": ([P, I, P, I, P, P], I),
         "hs_resolve_ce": ([P, P, I, P, P], I),
         "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
         "hs_host_pool": ([P], P),
@@ -166,6 +168,27 @@ def hs_destroy(h: int) -> None:
 def hs_resolve(h: int, topk_idx, K: int, out_slot, stream=None) -> None:
     _check(lib.hs_resolve(h, _ptr(topk_idx), int(K), _ptr(out_slot), _stream(stream)),
            "hs_resolve")
+
+
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * max(len(xs), 1))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def hs_resolve_layers_rc(handles, topk_idx, K: int, out_slot, stream=None) -> int:
+    """handles, topk_idx and out_slot: sequences of L entries (one per layer)."""
+    L = len(handles)
+    if len(topk_idx) != L or len(out_slot) != L:
+        return HS_ERR_ARG
+    return lib.hs_resolve_layers(_ptr_array(handles), L, _ptr_array(topk_idx), int(K),
+                                 _ptr_array(out_slot), _stream(stream))
+
+
+def hs_resolve_layers(handles, topk_idx, K: int, out_slot, stream=None) -> None:
+    """L independent layers' step in one launch; same results as hs_resolve per layer."""
+    _check(hs_resolve_layers_rc(handles, topk_idx, K, out_slot, stream), "hs_resolve_layers")
 
 
 def hs_resolve_rc(h: int, topk_idx, K: int, out_slot, stream=None) -> int:

@@ -97,15 +97,26 @@ class GpuWorkload:
         return self.out[layer, step] if self.record else self.out[layer]
 
     def launch_step(self, s: int, stream=None, copy_engine: bool = False,
-                    layer_streams=None) -> int:
+                    layer_streams=None, one_launch: bool = False) -> int:
         """Enqueue step s for every layer; returns the number of kernel launches.
 
         ``copy_engine`` uses the copy-engine comparison variant (hs_resolve_ce),
         which synchronises the stream inside every call.  ``layer_streams``
         (one torch stream per layer) runs the independent layers concurrently:
         each waits for ``stream`` at the start and ``stream`` waits for all of
-        them at the end, so one layer's resolve overlaps another's row fetch."""
+        them at the end, so one layer's resolve overlaps another's row fetch.
+        ``one_launch`` resolves all layers in one launch (hs_resolve_layers)."""
         wl = self.wl
+        if one_launch:
+            n = 0
+            if self.append_rows is not None:
+                for layer, h in enumerate(self.handles):
+                    hs.hs_append(h.h, self.append_rows[layer, s], stream)
+                    n += 1
+            L = len(self.handles)
+            hs.hs_resolve_layers([h.h for h in self.handles], [self.topk[l, s] for l in range(L)],
+                                 wl.K, [self.out_at(l, s) for l in range(L)], stream)
+            return n + 1
         if layer_streams is not None:
             main = stream if stream is not None else torch.cuda.current_stream()
             fork = torch.cuda.Event()

@@ -93,6 +93,7 @@ typedef struct CUstream_st* hs_stream_t;
 #define HS_MAX_SLOTS      16384
 #define HS_MAX_BATCH      4096
 #define HS_MAX_ROW_BYTES  65536
+#define HS_MAX_LAYERS     16      /* handles per hs_resolve_layers call */
 
 typedef struct {
     int64_t steps;         /* resolves issued on the handle (its step counter) */
@@ -146,6 +147,25 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
  */
 int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_t* out_slot,
                      hs_stream_t stream);
+
+/*
+ * The step of L independent layers in one launch.  The pages name better
+ * overlap of the miss I/O with other work as the way to cut its overhead
+ * (HiSparse blog, section "今後の展望" (outlook)): here the CTAs of all
+ * layers share the GPU, so while some resolve their tables others fetch
+ * rows, and a layer's idle start is hidden behind the others' copies.
+ * handles, topk_idx and out_slot are HOST arrays of L entries: handle l
+ * resolves topk_idx[l] (device, [B][K]) into out_slot[l] (device, [B][K])
+ * with exactly the result of hs_resolve on that handle.  The handles must be
+ * distinct, made on one device, and share B, S and row_bytes; their
+ * context length, tail, policy and tail mode may differ.  One fused launch of
+ * L * B CTAs whatever the handles' copy mode.  1 <= L <= HS_MAX_LAYERS,
+ * 1 <= K <= min(S, HS_MAX_TOPK).  Asynchronous; graph-capturable.  Errors:
+ * HS_ERR_ARG (a NULL array, entry or handle, a handle given twice, shapes
+ * that differ, another device), HS_ERR_TOPK_GT_SLOTS, HS_ERR_LIMIT.
+ */
+int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
+                      int32_t* const* out_slot, hs_stream_t stream);
 
 /*
  * The same step from host memory: topk_idx (host, [B][K]) in, out_slot (host,

@@ -22,11 +22,13 @@ class GpuResult:
 
 
 def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO,
-            policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False):
-    """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one."""
+            policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False, one_launch=False):
+    """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one.
+
+    ``policy`` is one eviction policy for every layer, or a list with one per layer."""
     w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
-    for h in w.handles:
-        hs.hs_set_policy(h.h, policy)
+    for layer, h in enumerate(w.handles):
+        hs.hs_set_policy(h.h, policy[layer] if isinstance(policy, (list, tuple)) else policy)
     res_policy = policy
     if setup is not None:
         setup(w)
@@ -46,14 +48,16 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for s in range(steps):
-                w.launch_step(s, torch.cuda.current_stream(), layer_streams=lstreams)
+                w.launch_step(s, torch.cuda.current_stream(), layer_streams=lstreams,
+                              one_launch=one_launch)
         g.replay()
         torch.cuda.synchronize()
         res.misses = None  # per-step counts are not observable inside one graph
     else:
         with torch.cuda.stream(stream):
             for s in range(steps):
-                w.launch_step(s, stream, copy_engine=copy_engine, layer_streams=lstreams)
+                w.launch_step(s, stream, copy_engine=copy_engine, layer_streams=lstreams,
+                              one_launch=one_launch)
                 for layer, h in enumerate(w.handles):
                     hs.hs_stats(h.h, res.misses[layer, s])
     torch.cuda.synchronize()
@@ -97,8 +101,11 @@ def compare(wl, res, requests=None, layers=None):
 
     def one(job):
         layer, b = job
+        policy = getattr(res, "policy", 0)
+        if isinstance(policy, (list, tuple)):
+            policy = policy[layer]
         st, outs, counts, errs = oracle_request(wl, layer, b, res.trace[layer, :, b], steps,
-                                                policy=getattr(res, "policy", 0))
+                                                policy=policy)
         tok, slot_tok, stamp, step = res.state[layer]
         ctx = "layer %d request %d" % (layer, b)
         np.testing.assert_array_equal(res.out[layer, :, b], outs, err_msg=ctx + " out_slot")

@@ -75,3 +75,13 @@ def test_null_handle_is_rejected(hs):
     assert hs.lib.hs_h2d_read(None, None, 16, 0, None) == hs.HS_ERR_ARG
     assert hs.lib.hs_h2d_read(1, 1, 15, 0, None) == hs.HS_ERR_ARG
     hs.hs_destroy(None)  # no-op
+
+
+def test_resolve_layers_host_checks(hs):
+    rc = hs.hs_resolve_layers_rc
+    assert rc([], [], 4, []) == hs.HS_ERR_ARG
+    assert rc([None], [1], 4, [1]) == hs.HS_ERR_ARG
+    assert rc([1], [1], 0, [1]) == hs.HS_ERR_ARG
+    n = hs.HS_MAX_LAYERS + 1
+    assert rc([1] * n, [1] * n, 4, [1] * n) == hs.HS_ERR_LIMIT
+    assert hs.lib.hs_resolve_layers(None, 1, None, 4, None, None) == hs.HS_ERR_ARG

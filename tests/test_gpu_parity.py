@@ -83,6 +83,59 @@ def test_parity_layers_on_concurrent_streams(graph):
         res.workload.close()
 
 
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_parity_layers_in_one_launch(graph):
+    """The four layers' step as one grid (hs_resolve_layers)."""
+    from gpu_harness import compare, gpu_run
+    wl = tg.WORKLOADS["b64_c128k_l4_tail4096"]
+    res = gpu_run(wl, steps=40, graph=graph, one_launch=True)
+    try:
+        compare(wl, res, requests=[0, 21, 63])
+    finally:
+        res.workload.close()
+
+
+def test_parity_one_launch_mixed_layers():
+    """One launch over layers that differ in policy, with a sliding tail fed by
+    appends; every request of every layer against the oracle."""
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = tg.Workload("layers_slide", 87, B=6, C=6144, K=384, S=768, T=256, host_ratio=8,
+                     layers=3, steps=120, len0=3000, grow=1, carry_pct=60, zipf_pct=30,
+                     third=tg.THIRD_RECENT, recent=1024, sliding=True)
+    res = gpu_run(wl, one_launch=True, policy=[hs.HS_POLICY_LRU, hs.HS_POLICY_FIFO,
+                                               hs.HS_POLICY_LRU])
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+        assert tot[1] > 0 and tot[2] > 0
+    finally:
+        res.workload.close()
+
+
+def test_one_launch_argument_checks():
+    from hierarchical_kv_cache_hs_gb300 import hs
+    a = hs.Handle(4, 2048, 64, 256, 8)
+    b = hs.Handle(4, 2048, 64, 256, 8)
+    c = hs.Handle(4, 2048, 64, 512, 4)   # other S
+    d = hs.Handle(2, 2048, 64, 256, 8)   # other B
+    try:
+        t = torch.arange(128, dtype=torch.int32, device="cuda").repeat(4, 1).contiguous()
+        o = torch.empty_like(t)
+        rc = hs.hs_resolve_layers_rc
+        assert rc([a.h, a.h], [t, t], 128, [o, o]) == hs.HS_ERR_ARG
+        assert rc([a.h, c.h], [t, t], 128, [o, o]) == hs.HS_ERR_ARG
+        assert rc([a.h, d.h], [t, t], 128, [o, o]) == hs.HS_ERR_ARG
+        assert rc([a.h, b.h], [t, None], 128, [o, o]) == hs.HS_ERR_ARG
+        assert rc([a.h, b.h], [t, t], 257, [o, o]) == hs.HS_ERR_TOPK_GT_SLOTS
+        assert rc([a.h, b.h], [t, t], 128, [o, o]) == hs.HS_OK
+        torch.cuda.synchronize()
+        assert a.stats()["misses"] == 4 * 128 and b.stats()["misses"] == 4 * 128
+    finally:
+        for h in (a, b, c, d):
+            h.close()
+
+
 EDGE = {
     # ragged: K and S not multiples of the CTA width, B odd
     "ragged": tg.Workload("ragged", 91, B=3, C=5000, K=1000, S=3000, T=0, host_ratio=2, layers=1,
