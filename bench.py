@@ -42,6 +42,10 @@ PRIME_STEPS = 10
 # host-link bytes equal the algorithmic miss-row bytes of that launch.
 FUSED_NCU_DRAM_BYTES = 9065472 + 886272
 FUSED_NCU_SYSMEM_BYTES = 933264 * 32
+# The same for the one-launch layers kernel on the 4-layer, 64-request,
+# 128K-context workload (profiles/hs_resolve_layers_kernel_b64_c128k_l4.md).
+LAYERS_NCU_DRAM_BYTES = 44859904 + 68583680
+LAYERS_NCU_SYSMEM_BYTES = 3410100 * 32
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -463,10 +467,14 @@ def run_ours(args, rank, world, dist):
                      "achieved": copy_gbs,
                      "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
                      # ncu, one steady-state launch of this kernel on this workload
-                     # (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md); None when
-                     # another kernel or workload is timed
-                     "traffic": FUSED_NCU_DRAM_BYTES if (fused and wl.name == "b64_c64k_s4096") else None,
-                     "traffic_host_link": FUSED_NCU_SYSMEM_BYTES if (fused and wl.name == "b64_c64k_s4096") else None,
+                     # (the summaries under profiles/); None when another kernel or
+                     # workload is timed
+                     "traffic": (FUSED_NCU_DRAM_BYTES if (fused and not one and wl.name == "b64_c64k_s4096")
+                                 else LAYERS_NCU_DRAM_BYTES if (one and wl.name == "b64_c128k_l4_tail4096")
+                                 else None),
+                     "traffic_host_link": (FUSED_NCU_SYSMEM_BYTES if (fused and not one and wl.name == "b64_c64k_s4096")
+                                           else LAYERS_NCU_SYSMEM_BYTES if (one and wl.name == "b64_c128k_l4_tail4096")
+                                           else None),
                      "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
                                     "1 GiB zero-copy 128-bit read kernel)"},
         "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if (fused or one) else
