@@ -13,9 +13,10 @@ import pytest
 
 import oracle
 
-# Not listed: dropping the explicit "skip slots hit this step" from the victim
-# candidates is an equivalent change, because hit slots already carry this
-# step's stamp (the newest) and K <= S leaves enough older slots.
+# Dropping the explicit "skip slots hit this step" from the victim candidates
+# is an equivalent change under LRU (hit slots already carry this step's
+# stamp, the newest, and K <= S leaves enough older slots), but not under FIFO,
+# where a hit keeps its old fill stamp: "fifo_hit_slots_evictable" plants it.
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "hs_oracle.c")
 
@@ -38,16 +39,28 @@ MUTANTS = {
     "sliding_no_write_back": ("if (t >= T) memcpy(host", "if (0) memcpy(host"),
     "sliding_fixed_boundary": ("sliding ? (len - T > 0 ? len - T : 0) : C - T", "C - T"),
     "alias_repeats_unresolved": ("out[j] = out[alias_of[j]];", "out[j] = -1;"),
+    "fifo_hit_slots_evictable": ("if (hit[s]) continue;", "if (0) continue;"),
+    "evict_newest_first": ("if (x->stamp != y->stamp) return x->stamp < y->stamp ? -1 : 1;",
+                           "if (x->stamp != y->stamp) return x->stamp > y->stamp ? -1 : 1;"),
+    "misses_paired_reversed": [("int32_t t = miss_tok[i];", "int32_t t = miss_tok[nmiss - 1 - i];"),
+                               ("out[miss_pos[i]] = v;", "out[miss_pos[nmiss - 1 - i]] = v;")],
+    "short_row_copy": ("(size_t)t * (size_t)R, (size_t)R);", "(size_t)t * (size_t)R, (size_t)R - 1);"),
+    "tail_boundary_off_by_one": ("if (t >= cold) {", "if (t > cold) {"),
+    "padding_flagged": ("if (t == -1) continue;", "if (t == -1) { err |= OR_E_RANGE; continue; }"),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_reject_planted_mistake(tmp_path, name):
-    old, new = MUTANTS[name]
+    edits = MUTANTS[name]
+    if isinstance(edits, tuple):
+        edits = [edits]
     src = open(SRC).read()
-    assert src.count(old) == 1, name
+    for old, new in edits:
+        assert src.count(old) == 1, name
+        src = src.replace(old, new)
     path = tmp_path / ("mut_%s.c" % name)
-    path.write_text(src.replace(old, new))
+    path.write_text(src)
     so = tmp_path / ("libmut_%s.so" % name)
     subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-w", str(path), "-o", str(so)],
                    check=True)
@@ -61,6 +74,9 @@ def test_pins_reject_planted_mistake(tmp_path, name):
         "try:\n"
         "    check_golden(oracle, lib=lib)\n"
         "    check_against_simulator(oracle, range(400), lib=lib)\n"
+        "    check_against_simulator(oracle, range(150), lib=lib, fifo=True)\n"
+        "    check_against_simulator(oracle, range(150), lib=lib, sliding=True)\n"
+        "    check_against_simulator(oracle, range(150), lib=lib, alias=True)\n"
         "except AssertionError:\n"
         "    sys.exit(3)\n"
         "sys.exit(0)\n" % (here, os.path.dirname(here), str(so)))
