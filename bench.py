@@ -584,9 +584,14 @@ def cpu_baseline(wl, args, total_steps):
     from_step = PRIME_STEPS + args.warmup
     secs = _oracle_requests(wl, total_steps, list(range(wl.B)), cores, from_step)
     n = wl.B * (total_steps - from_step)
+    # The same on one core, over the first few requests.
+    nb1 = min(8, wl.B)
+    secs1 = _oracle_requests(wl, total_steps, list(range(nb1)), 1, from_step)
     return {"value": n / secs, "unit": "resolves/s", "cores": cores, "kind": "oracle",
             "sample": "the timed steps of the same trace, all %d requests, one request per thread "
-                      "per step, after replaying the untimed prefix" % wl.B}
+                      "per step, after replaying the untimed prefix" % wl.B,
+            "single_core": {"value": nb1 * (total_steps - from_step) / secs1, "unit": "resolves/s",
+                            "cores": 1, "sample": "the same timed steps, requests 0-%d" % (nb1 - 1)}}
 
 
 def run_reference(args):
