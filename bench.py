@@ -208,6 +208,15 @@ class RankOps:
         return self._reduce(x, None if self.dist is None else self.dist.ReduceOp.SUM)
 
 
+def _quantiles(xs):
+    """min, 10 %, median, 90 %, max of the per-step times, and the means of the first and last tenth."""
+    v = sorted(xs)
+    n = len(v)
+    k = max(1, n // 10)
+    return {"min": v[0], "p10": v[n // 10], "p50": v[n // 2], "p90": v[(9 * n) // 10], "max": v[-1],
+            "first_tenth_mean": sum(xs[:k]) / k, "last_tenth_mean": sum(xs[-k:]) / k}
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, dist):
     import torch
@@ -490,6 +499,7 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": main["launches"],
         "clocks": clocks,
         "wall_s_timed_region": main["wall_s"],
+        "step_ms_quantiles": _quantiles(main["step_ms"]),
     }
     if args.overlap and rank == 0:
         line["layer_overlap"] = layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev)
