@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libhs.so")
 
 SOURCES = ["hs_api.cpp", "hs_resolve.cu", "hs_copy.cu", "hs_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "hs_internal.h"), os.path.join(INCLUDE, "hs.h")]
+HEADERS = [os.path.join(CSRC, "hs_internal.h"), os.path.join(CSRC, "hs_gather_pool.h"),
+           os.path.join(INCLUDE, "hs.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -3,90 +3,14 @@
 // data on the resolve path; everything it enqueues is graph-capturable.
 #include <cuda_runtime.h>
 
-#include <atomic>
-#include <condition_variable>
 #include <cstdlib>
 #include <cstring>
 #include <functional>
-#include <mutex>
 #include <new>
 #include <thread>
-#include <vector>
 
+#include "hs_gather_pool.h"
 #include "hs_internal.h"
-
-namespace {
-
-// A fixed set of host threads that run `fn(task)` for every task of a batch
-// and return when all are done (used by the copy-engine variant's gather).
-class GatherPool {
-public:
-    explicit GatherPool(int n)
-    {
-        for (int i = 0; i < n; ++i) threads_.emplace_back([this] { loop(); });
-    }
-    ~GatherPool()
-    {
-        {
-            std::lock_guard<std::mutex> g(mu_);
-            stop_ = true;
-        }
-        cv_.notify_all();
-        for (auto& t : threads_) t.join();
-    }
-    void run(int ntasks, const std::function<void(int)>& fn)
-    {
-        if (ntasks <= 0) return;
-        std::unique_lock<std::mutex> g(mu_);
-        fn_ = &fn;
-        ntasks_ = ntasks;
-        next_.store(0);
-        left_ = ntasks;
-        ++gen_;
-        cv_.notify_all();
-        done_.wait(g, [this] { return left_ == 0; });
-        fn_ = nullptr;
-    }
-
-private:
-    void loop()
-    {
-        unsigned long long seen = 0;
-        for (;;) {
-            const std::function<void(int)>* fn;
-            int n;
-            {
-                std::unique_lock<std::mutex> g(mu_);
-                cv_.wait(g, [&] { return stop_ || gen_ != seen; });
-                if (stop_) return;
-                seen = gen_;
-                fn = fn_;
-                n = ntasks_;
-            }
-            int done = 0;
-            for (int t = next_.fetch_add(1); t < n; t = next_.fetch_add(1)) {
-                (*fn)(t);
-                ++done;
-            }
-            if (done) {
-                std::lock_guard<std::mutex> g(mu_);
-                left_ -= done;
-                if (left_ == 0) done_.notify_all();
-            }
-        }
-    }
-    std::vector<std::thread> threads_;
-    std::mutex mu_;
-    std::condition_variable cv_, done_;
-    const std::function<void(int)>* fn_ = nullptr;
-    int ntasks_ = 0;
-    int left_ = 0;
-    std::atomic<int> next_{0};
-    unsigned long long gen_ = 0;
-    bool stop_ = false;
-};
-
-}  // namespace
 
 struct hs_handle {
     int B, C, R, S, T, H, cold;
