@@ -48,7 +48,9 @@ __global__ void __launch_bounds__(CT) hs_copy_kernel(CopyArgs a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (a.advance_step && blockIdx.x == 0 && tid == 0) a.st->step = (int)((unsigned)a.st->step + 1u);  // wraps; the next step repairs it
+    // Advance the step counter (wrapping: the next resolve clamps a counter
+    // outside its range and reports it).
+    if (a.advance_step && blockIdx.x == 0 && tid == 0) a.st->step = (int)((unsigned)a.st->step + 1u);
 
     // Exclusive prefix of the miss counts over requests.
     int carry = 0;
