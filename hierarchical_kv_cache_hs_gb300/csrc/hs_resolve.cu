@@ -222,6 +222,27 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     }
     if (a.fifo)
         for (int i = tid; i < ((S + 31) >> 5); i += NT) s_hitbits[i] = 0u;
+    // ---- (1) classify, gather the page table, find repeats ----------------
+    // The page-table gathers are issued before waiting for the stamp rows, so
+    // their DRAM latency overlaps the wait.
+    int cl[EMAX], hs[EMAX], sl[EMAX];
+    int err = 0;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int t = tk[e];
+        cl[e] = C_NONE;
+        sl[e] = -1;
+        hs[e] = 0;
+        if (e < E && j0 + e < K && t != -1) {
+            if (t < -1 || t >= len || t >= a.C) {
+                cl[e] = C_BAD;
+                err |= HS_E_RANGE;
+            } else {
+                cl[e] = C_MISS;  // valid; refined below
+                if (t < cold) sl[e] = g_tok_slot[t];
+            }
+        }
+    }
     if (vec_rows) cp_async_wait_all();
     // Every stamp must lie in [0, step - 1] for the victim search to place
     // exactly m victims: each thread clamps the stamps it loaded itself (as
@@ -247,28 +268,10 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             }
         }
     }
+    err |= bad_state;
     if (tid < 3) s_cnt[tid] = 0;
     __syncthreads();
 
-    // ---- (1) classify, gather the page table, find repeats ----------------
-    int cl[EMAX], hs[EMAX], sl[EMAX];
-    int err = bad_state;
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-        const int t = tk[e];
-        cl[e] = C_NONE;
-        sl[e] = -1;
-        hs[e] = 0;
-        if (e < E && j0 + e < K && t != -1) {
-            if (t < -1 || t >= len || t >= a.C) {
-                cl[e] = C_BAD;
-                err |= HS_E_RANGE;
-            } else {
-                cl[e] = C_MISS;  // valid; refined below
-                if (t < cold) sl[e] = g_tok_slot[t];
-            }
-        }
-    }
     // Repeated indices: the first occurrence in row order wins.  A resident
     // token claims its slot by raising the slot's stamp word to
     // step + K - j (the largest value belongs to the smallest j); every other
