@@ -95,14 +95,16 @@ def test_parity_layers_in_one_launch(graph):
         res.workload.close()
 
 
-def test_parity_one_launch_mixed_layers():
+@pytest.mark.parametrize("row_bytes", [1152, 1040])
+def test_parity_one_launch_mixed_layers(row_bytes):
     """One launch over layers that differ in policy, with a sliding tail fed by
-    appends; every request of every layer against the oracle."""
+    appends; every request of every layer against the oracle (both copy
+    unrolls)."""
     from gpu_harness import check_counters, compare, gpu_run
     from hierarchical_kv_cache_hs_gb300 import hs
     wl = tg.Workload("layers_slide", 87, B=6, C=6144, K=384, S=768, T=256, host_ratio=8,
                      layers=3, steps=120, len0=3000, grow=1, carry_pct=60, zipf_pct=30,
-                     third=tg.THIRD_RECENT, recent=1024, sliding=True)
+                     third=tg.THIRD_RECENT, recent=1024, sliding=True, row_bytes=row_bytes)
     res = gpu_run(wl, one_launch=True, policy=[hs.HS_POLICY_LRU, hs.HS_POLICY_FIFO,
                                                hs.HS_POLICY_LRU])
     try:
@@ -157,6 +159,22 @@ EDGE = {
     "small_rows": tg.Workload("small_rows", 95, B=300, C=2048, K=64, S=128, T=0, host_ratio=16,
                               layers=1, steps=25, len0=2048, grow=0, carry_pct=50, zipf_pct=25,
                               third=tg.THIRD_UNIFORM, row_bytes=16),
+    # rows of 65 16-byte chunks: the 8-deep copy unroll, row groups that end mid-warp;
+    # fused (20 requests) and split (5 requests)
+    "odd_rows_fused": tg.Workload("odd_rows_fused", 85, B=20, C=3000, K=300, S=600, T=0,
+                                  host_ratio=5, layers=1, steps=30, len0=3000, grow=0, carry_pct=60,
+                                  zipf_pct=30, third=tg.THIRD_ZIPF, row_bytes=1040),
+    "odd_rows_split": tg.Workload("odd_rows_split", 84, B=5, C=3000, K=300, S=600, T=0,
+                                  host_ratio=5, layers=1, steps=30, len0=3000, grow=0, carry_pct=60,
+                                  zipf_pct=30, third=tg.THIRD_ZIPF, row_bytes=1040),
+    # 2 KB rows with a resident tail
+    "wide_rows_tail": tg.Workload("wide_rows_tail", 83, B=17, C=4096, K=256, S=512, T=64,
+                                  host_ratio=8, layers=1, steps=25, len0=4096, grow=0, carry_pct=60,
+                                  zipf_pct=30, third=tg.THIRD_ZIPF, row_bytes=2048),
+    # the largest row (64 KB): one row per warp group, many chunks per lane, no early fetch
+    "max_rows": tg.Workload("max_rows", 82, B=16, C=512, K=64, S=128, T=0, host_ratio=4,
+                            layers=1, steps=10, len0=512, grow=0, carry_pct=50, zipf_pct=30,
+                            third=tg.THIRD_ZIPF, row_bytes=65536),
 }
 
 
