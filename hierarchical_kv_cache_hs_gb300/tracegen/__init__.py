@@ -164,6 +164,12 @@ WORKLOADS = {
     "b64_c128k_l4_tail4096": Workload("b64_c128k_l4_tail4096", 5, B=64, C=131072, K=2048, S=6144,
                                       T=4096, host_ratio=21, layers=4, steps=256, len0=131072,
                                       grow=0, carry_pct=70, zipf_pct=30, third=THIRD_ZIPF),
+    # Stress case beyond the five: the 4-layer shape without a tail, the 30 % of
+    # each row that is not carried over drawn uniformly over the whole context,
+    # so misses land anywhere in four 10 GB host pools.
+    "b64_c128k_l4_uniform": Workload("b64_c128k_l4_uniform", 5, B=64, C=131072, K=2048, S=6144,
+                                     T=0, host_ratio=22, layers=4, steps=256, len0=131072,
+                                     grow=0, carry_pct=70, zipf_pct=0, third=THIRD_UNIFORM),
 }
 
 

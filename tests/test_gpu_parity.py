@@ -96,6 +96,20 @@ def test_parity_layers_in_one_launch(graph):
 
 
 @pytest.mark.parametrize("row_bytes", [1152, 1040])
+def test_parity_uniform_misses_four_layers():
+    """Misses spread uniformly over four 10 GB host pools, all layers in one
+    launch; sampled requests of every layer against the oracle."""
+    from gpu_harness import compare, gpu_run
+    wl = tg.WORKLOADS["b64_c128k_l4_uniform"]
+    res = gpu_run(wl, steps=24, one_launch=True)
+    try:
+        tot, err = compare(wl, res, requests=[0, 37, 63])
+        assert tot[1] > 0 and err == 0
+    finally:
+        res.workload.close()
+
+
+@pytest.mark.parametrize("row_bytes", [1152, 1040])
 def test_parity_one_launch_mixed_layers(row_bytes):
     """One launch over layers that differ in policy, with a sliding tail fed by
     appends; every request of every layer against the oracle (both copy
