@@ -95,7 +95,6 @@ def test_parity_layers_in_one_launch(graph):
         res.workload.close()
 
 
-@pytest.mark.parametrize("row_bytes", [1152, 1040])
 def test_parity_uniform_misses_four_layers():
     """Misses spread uniformly over four 10 GB host pools, all layers in one
     launch; sampled requests of every layer against the oracle."""
