@@ -602,6 +602,29 @@ int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream)
     return HS_OK;
 }
 
+int hs_reset_requests(hs_handle* h, const int32_t* req_ids, int n, const int32_t* lengths,
+                      hs_stream_t stream)
+{
+    if (!valid(h) || n < 0 || (n > 0 && !req_ids)) return HS_ERR_ARG;
+    if (n > HS_MAX_BATCH) return HS_ERR_LIMIT;
+    if (n == 0) return HS_OK;
+    DeviceGuard g(h->device);
+    ResetArgs a;
+    a.ids = req_ids;
+    a.lengths = lengths;
+    a.tok_slot = h->d_tok_slot;
+    a.slot_tok = h->d_slot_tok;
+    a.stamp = h->d_stamp;
+    a.len = h->d_len;
+    a.st = h->d_st;
+    a.B = h->B;
+    a.C = h->C;
+    a.S = h->S;
+    if (hs_launch_reset_requests(a, n, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
 int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t* rows_host)
 {
     if (!valid(h) || !rows_host || b < 0 || b >= h->B || n < 0 || h->T <= 0) return HS_ERR_ARG;

@@ -12,8 +12,9 @@
 // zero-copy loads from the mapped host pool -- U independent loads in flight
 // per lane before the matching stores to HBM.
 //
-// Also here: the resident-tail append and a sequential host-read probe used
-// to measure the host->device link.
+// Also here: the resident-tail append, the reset of single requests (a batch
+// slot taken by a new request) and a sequential host-read probe used to
+// measure the host->device link.
 #include "hs_internal.h"
 
 namespace {
@@ -158,6 +159,27 @@ __global__ void hs_append_kernel(AppendArgs a)
     }
 }
 
+// One CTA per listed request: empty tables, stamps 0 ("never used", so the
+// request's slots are the first victims, lowest index first), new length.
+__global__ void hs_reset_requests_kernel(ResetArgs a)
+{
+    const int b = a.ids[blockIdx.x];
+    const int len = a.lengths ? a.lengths[blockIdx.x] : a.C;
+    if (b < 0 || b >= a.B || len < 0 || len > a.C) {
+        if (threadIdx.x == 0) atomicOr(&a.st->err, HS_E_RANGE);
+        return;
+    }
+    int32_t* ts = a.tok_slot + (size_t)b * a.C;
+    int32_t* sl = a.slot_tok + (size_t)b * a.S;
+    int32_t* sp = a.stamp + (size_t)b * a.S;
+    for (int t = threadIdx.x; t < a.C; t += blockDim.x) ts[t] = -1;
+    for (int v = threadIdx.x; v < a.S; v += blockDim.x) {
+        sl[v] = -1;
+        sp[v] = 0;
+    }
+    if (threadIdx.x == 0) a.len[b] = len;
+}
+
 constexpr int PROBE_U = 8;
 
 __global__ void __launch_bounds__(CT) hs_h2d_read_kernel(const uint8_t* src, uint8_t* dst,
@@ -229,6 +251,15 @@ cudaError_t hs_launch_append(const AppendArgs& a, int B, cudaStream_t s)
     cfg.blockDim = dim3(128);
     cfg.stream = s;
     return cudaLaunchKernelEx(&cfg, hs_append_kernel, a);
+}
+
+cudaError_t hs_launch_reset_requests(const ResetArgs& a, int n, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, hs_reset_requests_kernel, a);
 }
 
 cudaError_t hs_launch_h2d_read(const uint8_t* src, uint8_t* dst, size_t bytes, int grid,

@@ -77,6 +77,17 @@ struct AppendArgs {
     int sliding;
 };
 
+struct ResetArgs {
+    const int32_t* ids;      // [n] requests to reset
+    const int32_t* lengths;  // [n] or NULL (= C)
+    int32_t* tok_slot;
+    int32_t* slot_tok;
+    int32_t* stamp;
+    int32_t* len;
+    HsDevState* st;
+    int B, C, S;
+};
+
 // Launch geometry and shared-memory layout of the resolve kernel.
 constexpr int HS_RESOLVE_THREADS = 512;
 constexpr int HS_COPY_THREADS = 256;
@@ -122,5 +133,6 @@ int hs_copy_rows_per_group(int row_bytes, int unroll);
 int hs_copy_blocks_per_sm(int unroll, int B);
 
 cudaError_t hs_launch_append(const AppendArgs& a, int B, cudaStream_t s);
+cudaError_t hs_launch_reset_requests(const ResetArgs& a, int n, cudaStream_t s);
 cudaError_t hs_launch_h2d_read(const uint8_t* src, uint8_t* dst, size_t bytes, int grid,
                                cudaStream_t s);

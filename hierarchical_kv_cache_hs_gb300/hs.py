@@ -94,6 +94,7 @@ def _load():
         "hs_export_buffer": ([P, I, P], I),
         "hs_import_state": ([P, P, P, P, I], I),
         "hs_reset": ([P], I),
+        "hs_reset_requests": ([P, P, I, P, P], I),
         "hs_h2d_read": ([P, P, Z, I, P], I),
         "hs_profile_events": ([P, P, P], I),
         "hs_set_copy_mode": ([P, I], I),
@@ -279,6 +280,13 @@ def hs_export_buffer(h: int, b: int, dst_host) -> None:
 
 def hs_reset(h: int) -> None:
     _check(lib.hs_reset(h), "hs_reset")
+
+
+def hs_reset_requests(h: int, req_ids, n: int, lengths=None, stream=None) -> None:
+    """Empty the state of the n requests listed in req_ids (device int32 [n]),
+    with new lengths (device int32 [n]) or C; asynchronous on `stream`."""
+    _check(lib.hs_reset_requests(h, _ptr(req_ids), int(n), _ptr(lengths), _stream(stream)),
+           "hs_reset_requests")
 
 
 def hs_h2d_read(src_host, dst_dev, nbytes: int, blocks: int = 0, stream=None) -> None:

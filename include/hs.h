@@ -260,6 +260,23 @@ int hs_export_buffer(hs_handle* h, int b, uint8_t* dst_host);
 int hs_reset(hs_handle* h);
 
 /*
+ * Give batch slots to new requests (continuous batching).  A request starts
+ * with an empty hot buffer and loads rows only when the indexer selects them
+ * (vLLM Hybrid HiSparse post, "No Residency").  For each of the n entries of
+ * req_ids (device, int32 [n]), request b = req_ids[i] gets token->slot all -1,
+ * slot->token all -1, stamps 0 and length lengths[i] (device, int32 [n]; NULL
+ * means C).  Its host-pool rows and resident-tail rows are the caller's to
+ * write (hs_host_pool; hs_set_tail_rows or hs_append); its buffer bytes are
+ * left as they are and are never read before a miss refills them.  Other
+ * requests, the step counter and the counters are untouched.  An id outside
+ * [0, B) or a length outside [0, C] is skipped and latches HS_E_RANGE; a
+ * repeated id is reset once more.  0 <= n <= HS_MAX_BATCH.  Asynchronous and
+ * graph-capturable, ordered with the handle's other calls by the stream.
+ */
+int hs_reset_requests(hs_handle* h, const int32_t* req_ids, int n, const int32_t* lengths,
+                      hs_stream_t stream);
+
+/*
  * Measurement helper: stream `bytes` (a multiple of 16) from pinned host
  * memory `src_host` (allocated with cudaHostAlloc(..., cudaHostAllocMapped)
  * or returned by hs_host_pool) into device memory `dst_dev` with 128-bit

@@ -412,6 +412,64 @@ def test_corrupt_caller_state_is_contained(step0):
         h.close()
 
 
+def test_reset_requests_admits_new_requests():
+    """Continuous batching: after 12 steps, batch slots 1 and 4 take new
+    requests (slot 4 with a shorter length) and the run goes on.  Those
+    requests must match a fresh oracle state started at step 13; the others
+    must not notice.  An id outside the batch latches HS_E_RANGE only."""
+    import oracle
+    from gpu_harness import oracle_request
+    from hierarchical_kv_cache_hs_gb300 import hs
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+    wl = tg.Workload("admit", 81, B=6, C=5000, K=300, S=600, T=0, host_ratio=9, layers=1,
+                     steps=24, len0=5000, grow=0, carry_pct=60, zipf_pct=30, third=tg.THIRD_ZIPF)
+    w = GpuWorkload(wl, record=True)
+    try:
+        h = w.handles[0]
+        stream = torch.cuda.current_stream()
+        ids = torch.tensor([1, 4], dtype=torch.int32, device="cuda")
+        lens = torch.tensor([wl.C, wl.C - 100], dtype=torch.int32, device="cuda")
+        for s in range(wl.steps):
+            if s == 12:
+                hs.hs_reset_requests(h.h, ids, 2, lens, stream)
+            w.launch_step(s, stream)
+        torch.cuda.synchronize()
+        out = w.out.cpu().numpy()[0]
+        trace = w.topk.cpu().numpy()[0]
+        tok, slot_tok, stamp, step = h.export_state()
+        assert step == wl.steps
+        err = 0
+        for b in range(wl.B):
+            host = tg.rows(wl, 0, b, 0, wl.cold)
+            if b in (1, 4):
+                st1, o1, _, e1 = oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace[:12, b])
+                length = wl.C if b == 1 else wl.C - 100
+                st, o2, _, e2 = oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace[12:, b],
+                                                   length=length, step0=12)
+                outs = np.concatenate([o1, o2])
+                err |= int(np.bitwise_or.reduce(np.concatenate([e1, e2])))
+            else:
+                st, outs, _, e = oracle.run_request(wl.C, wl.S, wl.T, wl.row_bytes, host, trace[:, b])
+                err |= int(np.bitwise_or.reduce(e))
+            np.testing.assert_array_equal(out[:, b], outs, err_msg="request %d" % b)
+            np.testing.assert_array_equal(tok[b], st.tok_slot)
+            np.testing.assert_array_equal(slot_tok[b], st.slot_tok)
+            np.testing.assert_array_equal(stamp[b], st.stamp)
+            buf = h.export_buffer(b)
+            occ = np.nonzero(st.slot_tok >= 0)[0]
+            np.testing.assert_array_equal(buf[occ], st.buf[occ])
+        assert h.stats()["err_bits"] == err
+        # an id outside the batch: nothing changes but the error bit
+        bad = torch.tensor([wl.B + 3], dtype=torch.int32, device="cuda")
+        hs.hs_reset_requests(h.h, bad, 1, None, stream)
+        torch.cuda.synchronize()
+        tok2, slot_tok2, stamp2, _ = h.export_state()
+        assert (tok2 == tok).all() and (slot_tok2 == slot_tok).all() and (stamp2 == stamp).all()
+        assert h.stats()["err_bits"] & hs.HS_E_RANGE
+    finally:
+        w.close()
+
+
 def test_resolve_host_matches_device_path():
     from hierarchical_kv_cache_hs_gb300 import hs
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
