@@ -48,8 +48,12 @@
  * the handle's error word (HS_E_* bits, read by hs_stats).
  *
  * Streams: hs_stream_t is cudaStream_t (NULL = the legacy default stream).
- * hs_resolve and hs_append only enqueue work (no host synchronisation, no
+ * hs_resolve, hs_resolve_multi, hs_resolve_layers, hs_append and
+ * hs_reset_requests only enqueue work (no host synchronisation, no
  * allocation), so a sequence of them can be captured in a CUDA graph.
+ * Calls that read or set state from the host (hs_stats, hs_export_*,
+ * hs_import_state, hs_set_lengths, hs_set_tail_rows, hs_reset) synchronise
+ * the device first.
  */
 #ifndef HS_H
 #define HS_H
