@@ -557,51 +557,80 @@ def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
 
 
 # ---------------------------------------------------------------- CPU oracle
+ORACLE_HOST_BYTES = 8 << 30  # host rows the oracle legs may hold at once
+
+
+def _oracle_sample(wl):
+    """Requests the oracle legs replay: all of them, or the first n whose host
+    rows (every layer) fit in ORACLE_HOST_BYTES."""
+    per_request = wl.layers * wl.cold * wl.row_bytes
+    n = max(1, min(wl.B, ORACLE_HOST_BYTES // max(per_request, 1)))
+    return list(range(n))
+
+
 def _oracle_requests(wl, total_steps, requests, threads, time_from_step):
-    """Replay the trace on the CPU oracle; returns seconds spent on steps >= time_from_step."""
-    import numpy as np
+    """Replay the trace on the CPU oracle for the given requests of every
+    layer, appending each step's new token first on a growing context; returns
+    seconds spent on steps >= time_from_step."""
     import oracle
     from hierarchical_kv_cache_hs_gb300 import tracegen as tg
-    trace = tg.topk_trace(wl, steps=total_steps, requests=requests)
-    hosts = {}
+    jobs = [(layer, i) for layer in range(wl.layers) for i in range(len(requests))]
+    traces = [tg.topk_trace(wl, layer=layer, steps=total_steps, requests=requests)
+              for layer in range(wl.layers)]
+    hosts, appends = {}, {}
 
-    def prep(i):
-        b = requests[i]
-        hosts[i] = tg.rows(wl, 0, b, 0, wl.cold)
+    def prep(job):
+        layer, i = job
+        hosts[job] = tg.rows(wl, layer, requests[i], 0, wl.cold)
+        if wl.grow:
+            appends[job] = tg.rows(wl, layer, requests[i], wl.len0, total_steps)
 
-    oracle.parallel_map(prep, range(len(requests)), threads)
-    states = [oracle.RequestState(wl.C, wl.S, wl.T, wl.row_bytes) for _ in requests]
+    oracle.parallel_map(prep, jobs, threads)
+    length = wl.len0 if (wl.grow or wl.sliding) else wl.C
+    states = {job: oracle.RequestState(wl.C, wl.S, wl.T, wl.row_bytes, length, sliding=wl.sliding)
+              for job in jobs}
     from concurrent.futures import ThreadPoolExecutor
 
     elapsed = 0.0
     with ThreadPoolExecutor(threads) as ex:
         for s in range(total_steps):
-            def run(i, s=s):
-                states[i].resolve(hosts[i], trace[s, i], s + 1)
+            def run(job, s=s):
+                st = states[job]
+                if wl.grow:
+                    st.append(appends[job][s], hosts[job])
+                st.resolve(hosts[job], traces[job[0]][s, job[1]], s + 1)
             t0 = time.perf_counter()
-            list(ex.map(run, range(len(requests))))
+            list(ex.map(run, jobs))
             if s >= time_from_step:
                 elapsed += time.perf_counter() - t0
     return elapsed
 
 
+def _sample_desc(wl, requests):
+    who = "all %d requests" % wl.B if len(requests) == wl.B else "requests 0-%d of %d" % (
+        len(requests) - 1, wl.B)
+    layers = "" if wl.layers == 1 else " of each of the %d layers" % wl.layers
+    grow = ", each step's new token appended first" if wl.grow else ""
+    return who + layers + grow
+
+
 def cpu_baseline(wl, args, total_steps):
-    """The oracle as it stands, over all requests, on every host core."""
+    """The oracle as it stands on every host core (and on one), over a bounded
+    sample of the workload's requests."""
     cores = _cores()
-    if wl.layers != 1 or wl.grow:
-        return {"value": None, "unit": "resolves/s", "cores": cores, "kind": "oracle",
-                "sample": "not run for multi-layer / growing workloads"}
     from_step = PRIME_STEPS + args.warmup
-    secs = _oracle_requests(wl, total_steps, list(range(wl.B)), cores, from_step)
-    n = wl.B * (total_steps - from_step)
+    reqs = _oracle_sample(wl)
+    secs = _oracle_requests(wl, total_steps, reqs, cores, from_step)
+    n = len(reqs) * wl.layers * (total_steps - from_step)
     # The same on one core, over the first few requests.
-    nb1 = min(8, wl.B)
-    secs1 = _oracle_requests(wl, total_steps, list(range(nb1)), 1, from_step)
+    reqs1 = reqs[:min(8, len(reqs))]
+    secs1 = _oracle_requests(wl, total_steps, reqs1, 1, from_step)
     return {"value": n / secs, "unit": "resolves/s", "cores": cores, "kind": "oracle",
-            "sample": "the timed steps of the same trace, all %d requests, one request per thread "
-                      "per step, after replaying the untimed prefix" % wl.B,
-            "single_core": {"value": nb1 * (total_steps - from_step) / secs1, "unit": "resolves/s",
-                            "cores": 1, "sample": "the same timed steps, requests 0-%d" % (nb1 - 1)}}
+            "sample": "the timed steps of the same trace, %s, one request per thread per step, "
+                      "after replaying the untimed prefix" % _sample_desc(wl, reqs),
+            "single_core": {"value": len(reqs1) * wl.layers * (total_steps - from_step) / secs1,
+                            "unit": "resolves/s", "cores": 1,
+                            "sample": "the same timed steps, %s" % _sample_desc(wl, reqs1)}}
 
 
 def run_reference(args):
@@ -609,8 +638,9 @@ def run_reference(args):
     wl = tg.WORKLOADS[args.workload]
     total_steps = PRIME_STEPS + args.warmup + args.steps
     cores = _cores()
-    secs = _oracle_requests(wl, total_steps, list(range(wl.B)), cores, PRIME_STEPS + args.warmup)
-    units = wl.B * wl.layers * args.steps
+    reqs = _oracle_sample(wl)
+    secs = _oracle_requests(wl, total_steps, reqs, cores, PRIME_STEPS + args.warmup)
+    units = len(reqs) * wl.layers * args.steps
     value = units / secs
     return {
         "impl": "reference",
@@ -628,8 +658,8 @@ def run_reference(args):
         "data": "synthetic (seeded top-k traces and uniform random KV row bytes)",
         "config": {"workload": _workload_desc(wl), "prime_steps_untimed": PRIME_STEPS},
         "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": cores, "kind": "oracle",
-                         "sample": "every timed step of the workload, all %d requests, one request "
-                                   "per thread" % wl.B},
+                         "sample": "every timed step of the workload, %s, one request per thread"
+                                   % _sample_desc(wl, reqs)},
         "e2e": {"value": value, "unit": "resolves/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
