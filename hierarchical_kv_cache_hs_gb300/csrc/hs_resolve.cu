@@ -28,12 +28,18 @@
 //   FUSED   the CTA then updates the tables and copies its own missing rows
 //           from the mapped host pool into the buffer (zero-copy 128-bit
 //           loads, U in flight per lane); the last CTA to finish advances the
-//           step counter.  One launch per step.  (Reading the first rows into
-//           shared memory with cp.async while the victims are still chosen
-//           was measured slower: asynchronous copies from host memory are
-//           throttled, so issuing them stalled the CTA for tens of us.)
+//           step counter.  One launch per step.  Each warp loads its first
+//           row group into registers as soon as the miss list exists, so the
+//           host link is busy while the victims are chosen.  (Staging those
+//           rows in shared memory instead -- cp.async, or bulk copies on an
+//           mbarrier issued by a separate fetch warp -- was measured no
+//           faster.)
 //   !FUSED  the CTA writes the miss / victim lists to global memory for the
 //           grid-wide copy kernel (hs_copy.cu), which advances the counter.
+//
+// hs_resolve_kernel runs one handle's B CTAs; hs_resolve_layers_kernel runs
+// the same per-CTA body for several independent handles (layers) in one
+// grid, CTA x serving request x mod B of layer x / B.
 #include <climits>
 
 #include "hs_internal.h"
