@@ -355,14 +355,14 @@ def run_ours(args, rank, world, dist):
                 out_host = torch.empty((wl.layers, wl.B, wl.K), dtype=torch.int32).pin_memory()
                 with torch.cuda.stream(stream):
                     for s in range(PRIME_STEPS + args.warmup):
-                        w.host_step(s, out_host, stream)
+                        w.host_step(s, out_host, stream, one_launch=one)
                     e2e_s = 0.0
                     for i in range(args.steps):
                         s = PRIME_STEPS + args.warmup + i
                         flush.fill_(i & 0xFF)
                         stream.synchronize()
                         t0 = time.perf_counter()
-                        w.host_step(s, out_host, stream)
+                        w.host_step(s, out_host, stream, one_launch=one)
                         e2e_s += time.perf_counter() - t0
                 res.update(e2e_s=e2e_s)
         finally:
@@ -495,7 +495,8 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": e2e_value, "unit": "resolves/s",
                 "h2d_bytes_per_step": wl.layers * wl.B * wl.K * 4,
                 "d2h_bytes_per_step": wl.layers * wl.B * wl.K * 4,
-                "api": "hs_resolve_host (pinned host top-k in, host out_slot back, synchronised)"},
+                "api": ("hs_resolve_layers_host" if one else "hs_resolve_host") +
+                       " (pinned host top-k in, host out_slot back, synchronised)"},
         "gpu_launches": main["launches"],
         "clocks": clocks,
         "wall_s_timed_region": main["wall_s"],

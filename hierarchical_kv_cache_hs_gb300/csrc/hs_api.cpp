@@ -369,6 +369,54 @@ int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* to
     return HS_OK;
 }
 
+int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
+                           int32_t* const* out_slot, hs_stream_t stream)
+{
+    if (!handles || !topk_idx || !out_slot || L <= 0 || K <= 0) return HS_ERR_ARG;
+    if (L > HS_MAX_LAYERS) return HS_ERR_LIMIT;
+    const hs_handle* h0 = handles[0];
+    if (!valid(h0)) return HS_ERR_ARG;
+    for (int l = 0; l < L; ++l)
+        if (!valid(handles[l]) || !topk_idx[l] || !out_slot[l]) return HS_ERR_ARG;
+    if (K > h0->S) return HS_ERR_TOPK_GT_SLOTS;
+    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    DeviceGuard g(h0->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Device addresses of mapped buffers; the others go through each handle's
+    // staging buffers.
+    const int32_t* d_in[HS_MAX_LAYERS];
+    int32_t* d_out[HS_MAX_LAYERS];
+    bool staged_out[HS_MAX_LAYERS];
+    for (int l = 0; l < L; ++l) {
+        hs_handle* h = handles[l];
+        const size_t bytes = (size_t)h->B * (size_t)K * sizeof(int32_t);
+        void* p = nullptr;
+        if (cudaHostGetDevicePointer(&p, const_cast<int32_t*>(topk_idx[l]), 0) == cudaSuccess) {
+            d_in[l] = static_cast<const int32_t*>(p);
+        } else {
+            cudaGetLastError();
+            if (cudaMemcpyAsync(h->d_stage_in, topk_idx[l], bytes, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess)
+                return HS_ERR_CUDA;
+            d_in[l] = h->d_stage_in;
+        }
+        p = nullptr;
+        staged_out[l] = cudaHostGetDevicePointer(&p, out_slot[l], 0) != cudaSuccess;
+        if (staged_out[l]) cudaGetLastError();
+        d_out[l] = staged_out[l] ? h->d_stage_out : static_cast<int32_t*>(p);
+    }
+    const int rc = hs_resolve_layers(handles, L, d_in, K, d_out, stream);
+    if (rc != HS_OK) return rc;
+    for (int l = 0; l < L; ++l) {
+        if (!staged_out[l]) continue;
+        const size_t bytes = (size_t)handles[l]->B * (size_t)K * sizeof(int32_t);
+        if (cudaMemcpyAsync(out_slot[l], handles[l]->d_stage_out, bytes, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+            return HS_ERR_CUDA;
+    }
+    return cudaStreamSynchronize(s) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
 int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                   hs_stream_t stream)
 {

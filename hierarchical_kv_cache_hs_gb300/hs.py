@@ -81,6 +81,7 @@ def _load():
         "hs_resolve_host": ([P, P, I, P, P], I),
         "hs_resolve_multi": ([P, P, I, I, P, P], I),
         "hs_resolve_layers": ([P, I, P, I, P, P], I),
+        "hs_resolve_layers_host": ([P, I, P, I, P, P], I),
         "hs_resolve_ce": ([P, P, I, P, P], I),
         "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
         "hs_host_pool": ([P], P),
@@ -190,6 +191,16 @@ def hs_resolve_layers_rc(handles, topk_idx, K: int, out_slot, stream=None) -> in
 def hs_resolve_layers(handles, topk_idx, K: int, out_slot, stream=None) -> None:
     """L independent layers' step in one launch; same results as hs_resolve per layer."""
     _check(hs_resolve_layers_rc(handles, topk_idx, K, out_slot, stream), "hs_resolve_layers")
+
+
+def hs_resolve_layers_host(handles, topk_idx, K: int, out_slot, stream=None) -> None:
+    """hs_resolve_layers from host buffers (sequences of L addresses or arrays); synchronous."""
+    L = len(handles)
+    if len(topk_idx) != L or len(out_slot) != L:
+        raise HsError(HS_ERR_ARG, "hs_resolve_layers_host")
+    _check(lib.hs_resolve_layers_host(_ptr_array(handles), L, _ptr_array(topk_idx), int(K),
+                                      _ptr_array(out_slot), _stream(stream)),
+           "hs_resolve_layers_host")
 
 
 def hs_resolve_rc(h: int, topk_idx, K: int, out_slot, stream=None) -> int:

@@ -147,8 +147,9 @@ class GpuWorkload:
                 n += hs.hs_resolve_launches(h.h)
         return n
 
-    def host_step(self, s: int, out_host: torch.Tensor, stream=None) -> None:
-        """Step s from host buffers (hs_resolve_host), for end-to-end timing.
+    def host_step(self, s: int, out_host: torch.Tensor, stream=None, one_launch: bool = False) -> None:
+        """Step s from host buffers (hs_resolve_host, or hs_resolve_layers_host
+        with ``one_launch``), for end-to-end timing.
 
         The top-k rows and results are passed as raw addresses into the pinned
         [layers][steps][B][K] trace and the [layers][B][K] output."""
@@ -156,6 +157,15 @@ class GpuWorkload:
         row = wl.B * wl.K * 4
         base_in = self.topk_host.data_ptr()
         base_out = out_host.data_ptr()
+        if one_launch:
+            if self.append_rows is not None:
+                for layer, h in enumerate(self.handles):
+                    hs.hs_append(h.h, self.append_rows[layer, s], stream)
+            L = len(self.handles)
+            hs.hs_resolve_layers_host([h.h for h in self.handles],
+                                      [base_in + (layer * self.steps + s) * row for layer in range(L)],
+                                      wl.K, [base_out + layer * row for layer in range(L)], stream)
+            return
         for layer, h in enumerate(self.handles):
             if self.append_rows is not None:
                 hs.hs_append(h.h, self.append_rows[layer, s], stream)

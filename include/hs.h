@@ -172,6 +172,15 @@ int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* to
                       int32_t* const* out_slot, hs_stream_t stream);
 
 /*
+ * hs_resolve_layers from host memory: topk_idx[l] and out_slot[l] are host
+ * buffers ([B][K] each), with the same rules as hs_resolve_host (mapped
+ * pinned buffers are read and written by the kernel directly, others are
+ * staged); synchronises the stream before returning.  Not graph-capturable.
+ */
+int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
+                           int32_t* const* out_slot, hs_stream_t stream);
+
+/*
  * The same step from host memory: topk_idx (host, [B][K]) in, out_slot (host,
  * [B][K]) out; synchronises the stream before returning.  When both buffers
  * are page-locked and mapped into the device address space (cudaHostAlloc,

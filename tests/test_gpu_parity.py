@@ -412,6 +412,39 @@ def test_corrupt_caller_state_is_contained(step0):
         h.close()
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_layers_host_matches_device_path(pinned):
+    """hs_resolve_layers_host (host top-k in, host out_slot back) against
+    hs_resolve_layers on the same steps: identical slots and state."""
+    from hierarchical_kv_cache_hs_gb300 import hs
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+    wl = tg.Workload("layers_host", 80, B=8, C=4096, K=256, S=512, T=128, host_ratio=8, layers=3,
+                     steps=16, len0=4096, grow=0, carry_pct=60, zipf_pct=30, third=tg.THIRD_ZIPF)
+    a = GpuWorkload(wl, record=True)
+    b = GpuWorkload(wl, record=False)
+    try:
+        stream = torch.cuda.current_stream()
+        trace = a.topk.cpu()
+        if pinned:
+            trace = trace.pin_memory()
+        out = torch.empty((wl.layers, wl.B, wl.K), dtype=torch.int32)
+        if pinned:
+            out = out.pin_memory()
+        L = wl.layers
+        for s in range(wl.steps):
+            a.launch_step(s, stream, one_launch=True)
+            hs.hs_resolve_layers_host([h.h for h in b.handles], [trace[l, s] for l in range(L)], wl.K,
+                                      [out[l] for l in range(L)], stream)
+            torch.cuda.synchronize()
+            assert torch.equal(out, a.out[:, s].cpu()), s
+        for ha, hb in zip(a.handles, b.handles):
+            for x, y in zip(ha.export_state(), hb.export_state()):
+                np.testing.assert_array_equal(x, y)
+    finally:
+        a.close()
+        b.close()
+
+
 def test_reset_requests_admits_new_requests():
     """Continuous batching: after 12 steps, batch slots 1 and 4 take new
     requests (slot 4 with a shorter length) and the run goes on.  Those
