@@ -54,14 +54,11 @@ def test_error_strings(hs):
     ((4, 1024, 1152, 64, 16, -1), -1),       # negative tail
     ((4, 1024, 1152, 64, 16, 2048), -1),     # tail longer than the context
     ((4, 1024, 1152, 64, 15, 0), -3),        # 15 * 64 host rows < 1024 cold tokens
-    ((4, 1024, 1152, 64, 15, 64), 0),        # ... but enough once 64 tokens are resident
     ((5000, 1024, 1152, 64, 16, 0), -6),     # batch beyond the limit
     ((4, 1024, 1152, 20000, 1, 0), -6),      # slots beyond the limit
     ((4, 1024, 1 << 17, 64, 16, 0), -6),     # row beyond the limit
 ])
 def test_create_argument_checks(hs, args, code):
-    if code == 0:
-        pytest.skip("valid arguments need a GPU")
     rc, h = hs.hs_create_rc(*args)
     assert rc == code and not h
 

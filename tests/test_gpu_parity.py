@@ -128,6 +128,15 @@ def test_parity_one_launch_mixed_layers(row_bytes):
         res.workload.close()
 
 
+def test_create_accepts_a_pool_that_covers_the_cold_tokens():
+    """15 host rows per slot cannot hold 1024 cold tokens at 64 slots (the CPU
+    test checks the refusal), but with 64 tokens resident 960 are enough."""
+    from hierarchical_kv_cache_hs_gb300 import hs
+    rc, h = hs.hs_create_rc(4, 1024, 1152, 64, 15, 64)
+    assert rc == hs.HS_OK and h
+    hs.hs_destroy(h)
+
+
 def test_one_launch_argument_checks():
     from hierarchical_kv_cache_hs_gb300 import hs
     a = hs.Handle(4, 2048, 64, 256, 8)
