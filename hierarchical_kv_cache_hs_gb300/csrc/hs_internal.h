@@ -110,7 +110,6 @@ __host__ __device__ inline size_t hs_resolve_base_bytes(int K, int S, int hash_b
 {
     const size_t ints = (size_t)hs_resolve_region_a_ints(hash_bits) + 2u * (size_t)S + (size_t)K;
     size_t bytes = 4u * ints + 2u * 2u * (size_t)K;
-    bytes += 2u * (size_t)(K & 1);                          // keep the next word array aligned
     bytes += 4u * (size_t)((S + 31) >> 5);
     return bytes;
 }

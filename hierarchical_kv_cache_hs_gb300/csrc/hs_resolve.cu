@@ -175,7 +175,9 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     int* s_mtok = s_slot_tok + S;             // [K]
     uint16_t* s_mj = reinterpret_cast<uint16_t*>(s_mtok + K);  // [K]
     uint16_t* s_vic = s_mj + K;                                 // [K]
-    unsigned* s_hitbits = reinterpret_cast<unsigned*>(s_vic + K + (K & 1));  // [ceil(S/32)]
+    // The two uint16 arrays hold 2K entries (4K bytes), so the word array after
+    // them is 4-byte aligned for every K.
+    unsigned* s_hitbits = reinterpret_cast<unsigned*>(s_vic + K);  // [ceil(S/32)]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // State the caller owns (the allocation-free entry point) may be

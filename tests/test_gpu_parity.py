@@ -128,6 +128,49 @@ def test_parity_one_launch_mixed_layers(row_bytes):
         res.workload.close()
 
 
+def _random_workload(seed):
+    """A small seeded workload with random sizes, tail, growth and row size."""
+    import random
+    rng = random.Random(seed)
+    S = rng.choice([1, 7, 64, 300, 1024, 2500])
+    K = rng.randint(1, min(S, 900))
+    T = rng.choice([0, 0, 16, 128])
+    grow = T > 0 and rng.random() < 0.5
+    C = rng.randint(max(K, 8), 6000) + T
+    ratio = -(-(C - T) // S)  # enough host rows for the cold tokens
+    len0 = C - T if grow else C  # a growing context starts with an empty tail
+    R = rng.choice([16, 1152, 1040, 4096])
+    B = rng.choice([1, 3, 17, 40])
+    return tg.Workload("rand%d" % seed, 70 + seed, B=B, C=C, K=K, S=S, T=T, host_ratio=ratio,
+                       layers=1, steps=rng.randint(5, 40), len0=len0, grow=1 if grow else 0,
+                       carry_pct=rng.choice([0, 50, 80]), zipf_pct=rng.choice([0, 30]),
+                       third=rng.choice([tg.THIRD_ZIPF, tg.THIRD_UNIFORM]), row_bytes=R)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_parity_random_workloads(seed):
+    """Seeded random sizes (slots, top-k, tail, growth, row size, batch) in a
+    random launch mode and policy, every request against the oracle."""
+    import random
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _random_workload(seed)
+    rng = random.Random(1000 + seed)
+    # more appends than tail slots: the extra appends are refused and flagged
+    expect = hs.HS_E_APPEND if (wl.grow and wl.steps > wl.T) else 0
+    _run_and_compare(wl, copy_mode=rng.choice([0, 1, 2]), policy=rng.choice([0, 1]),
+                     expect_err=expect)
+
+
+def test_parity_two_thousand_steps():
+    """A long run: slots that go unused for more than 1023 steps leave the
+    exact-age bins, so the victim search takes its radix-select path in the
+    ordinary flow of steps."""
+    wl = tg.Workload("long_run", 79, B=3, C=20000, K=64, S=256, T=0, host_ratio=80, layers=1,
+                     steps=2000, len0=20000, grow=0, carry_pct=80, zipf_pct=20,
+                     third=tg.THIRD_ZIPF)
+    _run_and_compare(wl)
+
+
 def test_create_accepts_a_pool_that_covers_the_cold_tokens():
     """15 host rows per slot cannot hold 1024 cold tokens at 64 slots (the CPU
     test checks the refusal), but with 64 tokens resident 960 are enough."""
@@ -193,6 +236,11 @@ EDGE = {
     "wide_rows_tail": tg.Workload("wide_rows_tail", 83, B=17, C=4096, K=256, S=512, T=64,
                                   host_ratio=8, layers=1, steps=25, len0=4096, grow=0, carry_pct=60,
                                   zipf_pct=30, third=tg.THIRD_ZIPF, row_bytes=2048),
+    # an odd top-k: the shared word array after the two 16-bit arrays (FIFO's hit
+    # bitmap) must stay aligned
+    "odd_k": tg.Workload("odd_k", 78, B=17, C=4000, K=301, S=512, T=0, host_ratio=8, layers=1,
+                         steps=25, len0=4000, grow=0, carry_pct=60, zipf_pct=30,
+                         third=tg.THIRD_ZIPF),
     # the largest row (64 KB): one row per warp group, many chunks per lane, no early fetch
     "max_rows": tg.Workload("max_rows", 82, B=16, C=512, K=64, S=128, T=0, host_ratio=4,
                             layers=1, steps=10, len0=512, grow=0, carry_pct=50, zipf_pct=30,
@@ -291,7 +339,7 @@ def test_parity_other_launch_mode(name, mode):
 
 @pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 2),
                                        ("tiny_b1_c8k", 0), ("b256_c32k_grow_tail512", 0),
-                                       ("ragged", 1)])
+                                       ("ragged", 1), ("odd_k", 1), ("odd_k", 2)])
 def test_parity_fifo_policy(name, mode):
     """FIFO eviction (hits keep their fill stamp) against the oracle's FIFO."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
