@@ -129,36 +129,116 @@ def test_parity_one_launch_mixed_layers(row_bytes):
 
 
 def _random_workload(seed):
-    """A small seeded workload with random sizes, tail, growth and row size."""
+    """A small seeded workload with random sizes, tail (fixed or sliding),
+    growth, layers and row size."""
     import random
     rng = random.Random(seed)
     S = rng.choice([1, 7, 64, 300, 1024, 2500])
     K = rng.randint(1, min(S, 900))
     T = rng.choice([0, 0, 16, 128])
     grow = T > 0 and rng.random() < 0.5
+    sliding = grow and rng.random() < 0.5
     C = rng.randint(max(K, 8), 6000) + T
     ratio = -(-(C - T) // S)  # enough host rows for the cold tokens
-    len0 = C - T if grow else C  # a growing context starts with an empty tail
+    steps = rng.randint(5, 40)
+    if sliding:
+        len0 = rng.randint(min(T, C - 8), C - 8)  # the tail holds the last T tokens written
+        steps = min(steps, C - len0)
+    else:
+        len0 = C - T if grow else C  # a fixed tail starts empty when the context grows
     R = rng.choice([16, 1152, 1040, 4096])
     B = rng.choice([1, 3, 17, 40])
+    carry = rng.choice([0, 50, 80])
     return tg.Workload("rand%d" % seed, 70 + seed, B=B, C=C, K=K, S=S, T=T, host_ratio=ratio,
-                       layers=1, steps=rng.randint(5, 40), len0=len0, grow=1 if grow else 0,
-                       carry_pct=rng.choice([0, 50, 80]), zipf_pct=rng.choice([0, 30]),
-                       third=rng.choice([tg.THIRD_ZIPF, tg.THIRD_UNIFORM]), row_bytes=R)
+                       layers=rng.choice([1, 1, 2, 3]), steps=steps, len0=len0,
+                       grow=1 if grow else 0, carry_pct=carry, zipf_pct=rng.choice([0, 100 - carry - 10]),
+                       third=rng.choice([tg.THIRD_ZIPF, tg.THIRD_UNIFORM]), row_bytes=R,
+                       sliding=sliding)
 
 
 @pytest.mark.parametrize("seed", range(12))
-def test_parity_random_workloads(seed):
-    """Seeded random sizes (slots, top-k, tail, growth, row size, batch) in a
-    random launch mode and policy, every request against the oracle."""
+def test_parity_random_multi_position(seed):
+    """Seeded random draft-position steps: P rows per request that repeat one
+    another's tokens and carry padding, random sizes, launch mode and policy."""
     import random
+    import oracle
+    from hierarchical_kv_cache_hs_gb300 import hs
+    rng = random.Random(500 + seed)
+    P = rng.choice([2, 3, 4])
+    Kp = rng.randint(1, 300)
+    S = P * Kp + rng.choice([0, 1, 100, 1000])
+    C = rng.randint(P * Kp + 1, 9000)
+    R = rng.choice([16, 1152, 1040])
+    B = rng.choice([1, 5, 20])
+    steps = rng.randint(3, 25)
+    ratio = -(-C // S)
+    policy = rng.choice([0, 1])
+    wl = tg.Workload("multi%d" % seed, 60 + seed, B=B, C=C, K=Kp, S=S, T=0, host_ratio=ratio,
+                     layers=P, steps=steps, len0=C, grow=0, carry_pct=rng.choice([0, 60]),
+                     zipf_pct=30, third=tg.THIRD_ZIPF, row_bytes=R)
+    rows = [tg.topk_trace(wl, layer=p_) for p_ in range(P)]
+    nrng = np.random.default_rng(seed)
+    for p_ in range(1, P):  # later positions repeat tokens of the first
+        take = nrng.random(rows[p_].shape) < 0.4
+        pick = nrng.integers(0, Kp, size=rows[p_].shape)
+        rows[p_] = np.where(take, np.take_along_axis(rows[0], pick, axis=2), rows[p_])
+    trace = np.ascontiguousarray(np.concatenate(rows, axis=2))  # [steps][B][P*K]
+    trace[nrng.random(trace.shape) < 0.03] = -1  # padding
+    h = hs.Handle(B, C, R, S, ratio, 0)
+    try:
+        hs.hs_set_copy_mode(h.h, rng.choice([0, 1, 2]))
+        hs.hs_set_policy(h.h, policy)
+        pool = h.host_pool()
+        for b in range(B):
+            pool[b, :C] = tg.rows(wl, 0, b, 0, C)
+        dev = torch.from_numpy(trace).cuda()
+        out = torch.empty_like(dev)
+        for s in range(steps):
+            hs.hs_resolve_multi(h.h, dev[s], P, Kp, out[s])
+        torch.cuda.synchronize()
+        out = out.cpu().numpy()
+        tok, slot_tok, stamp, step = h.export_state()
+        stats = h.stats()
+        tot_m = 0
+        for b in range(B):
+            st = oracle.RequestState(C, S, 0, R, policy=policy)
+            host = pool[b, :C].copy()
+            for s in range(steps):
+                o, c, e = st.resolve(host, trace[s, b], s + 1, alias=True)
+                np.testing.assert_array_equal(out[s, b], o, err_msg="step %d request %d" % (s, b))
+                assert e == 0
+                tot_m += c[1]
+            np.testing.assert_array_equal(tok[b], st.tok_slot)
+            np.testing.assert_array_equal(slot_tok[b], st.slot_tok)
+            np.testing.assert_array_equal(stamp[b], st.stamp)
+            occ = np.nonzero(st.slot_tok >= 0)[0]
+            np.testing.assert_array_equal(h.export_buffer(b)[occ], st.buf[occ])
+        assert stats["misses"] == tot_m and stats["err_bits"] == 0 and step == steps
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("seed", range(64))
+def test_parity_random_workloads(seed):
+    """Seeded random sizes (slots, top-k, tail, growth, layers, row size,
+    batch) in a random launch mode and policy, every request of every layer
+    against the oracle."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
     from hierarchical_kv_cache_hs_gb300 import hs
     wl = _random_workload(seed)
     rng = random.Random(1000 + seed)
-    # more appends than tail slots: the extra appends are refused and flagged
-    expect = hs.HS_E_APPEND if (wl.grow and wl.steps > wl.T) else 0
-    _run_and_compare(wl, copy_mode=rng.choice([0, 1, 2]), policy=rng.choice([0, 1]),
-                     expect_err=expect)
+    mode = rng.choice([0, 1, 2])
+    policies = [rng.choice([0, 1]) for _ in range(wl.layers)]
+    one = wl.layers > 1 and rng.random() < 0.5
+    # more appends than fixed tail slots: the extra appends are refused and flagged
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, copy_mode=mode, policy=policies, one_launch=one)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+    finally:
+        res.workload.close()
 
 
 def test_parity_two_thousand_steps():
