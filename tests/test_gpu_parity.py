@@ -241,6 +241,41 @@ def test_parity_random_workloads(seed):
         res.workload.close()
 
 
+@pytest.mark.parametrize("seed", range(16))
+def test_parity_random_noisy_traces(seed):
+    """The random workloads with input errors mixed into every row: padding,
+    indices below -1 or past the current length, and repeats of an earlier
+    entry.  Those entries get -1 and the same error bits as the oracle; the
+    rest of the step is unaffected."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _random_workload(100 + seed)
+    rng = random.Random(2000 + seed)
+    trace = np.stack([tg.topk_trace(wl, layer=l) for l in range(wl.layers)])  # [L][steps][B][K]
+    nrng = np.random.default_rng(seed)
+    u = nrng.random(trace.shape)
+    trace[u < 0.03] = -1
+    trace[(u >= 0.03) & (u < 0.04)] = wl.C + 5                     # past any length
+    trace[(u >= 0.04) & (u < 0.045)] = -3                          # below -1
+    if wl.K > 1:  # repeats: copy an earlier entry of the same row
+        rep = (u >= 0.045) & (u < 0.07)
+        rep[..., 0] = False
+        idx = np.nonzero(rep)
+        trace[idx] = trace[idx[:-1] + (nrng.integers(0, idx[-1]),)] if len(idx[-1]) else trace[idx]
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, trace=trace, copy_mode=rng.choice([0, 1, 2]),
+                  policy=[rng.choice([0, 1]) for _ in range(wl.layers)],
+                  one_launch=wl.layers > 1 and rng.random() < 0.5)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+        if ((trace >= wl.C) | (trace < -1)).any():
+            assert err & hs.HS_E_RANGE
+    finally:
+        res.workload.close()
+
+
 def test_parity_two_thousand_steps():
     """A long run: slots that go unused for more than 1023 steps leave the
     exact-age bins, so the victim search takes its radix-select path in the
