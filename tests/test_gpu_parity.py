@@ -276,6 +276,53 @@ def test_parity_random_noisy_traces(seed):
         res.workload.close()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_noalloc_random_matches_handle_path(seed):
+    """hs_resolve_noalloc on caller-owned state against hs_resolve, on random
+    fixed-context sizes (with or without a resident tail)."""
+    import random
+    from hierarchical_kv_cache_hs_gb300 import hs
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+    k = 0
+    while True:  # the next random workload without growth, one layer
+        wl = _random_workload(300 + seed * 50 + k)
+        k += 1
+        if not wl.grow and not wl.sliding:
+            break
+    wl = wl.with_(layers=1)
+    ref = GpuWorkload(wl, record=True)
+    try:
+        h = ref.handles[0]
+        dev = "cuda"
+        B, C, S, T, R, K = wl.B, wl.C, wl.S, wl.T, wl.row_bytes, wl.K
+        tok_slot = torch.full((B, C), -1, dtype=torch.int32, device=dev)
+        slot_tok = torch.full((B, S), -1, dtype=torch.int32, device=dev)
+        stamp = torch.zeros((B, S), dtype=torch.int32, device=dev)
+        lengths = torch.full((B,), C, dtype=torch.int32, device=dev)
+        buf = torch.zeros((B, S + T, R), dtype=torch.uint8, device=dev)
+        control = torch.zeros(8, dtype=torch.int32, device=dev)
+        out = torch.full((wl.steps, B, K), -7, dtype=torch.int32, device=dev)
+        for b in range(T and B):
+            buf[b, S:] = torch.from_numpy(h.export_buffer(b)[S:]).to(dev)
+        stream = torch.cuda.current_stream()
+        for s in range(wl.steps):
+            ref.launch_step(s, stream)
+            hs.hs_resolve_noalloc(B, C, R, S, wl.H, T, ref.topk[0, s], K, out[s], tok_slot, slot_tok,
+                                  stamp, lengths, hs.hs_host_pool(h.h), buf, control, stream)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref.out[0])
+        tok_ref, slot_ref, stamp_ref, step_ref = h.export_state()
+        np.testing.assert_array_equal(tok_slot.cpu().numpy(), tok_ref)
+        np.testing.assert_array_equal(slot_tok.cpu().numpy(), slot_ref)
+        np.testing.assert_array_equal(stamp.cpu().numpy(), stamp_ref)
+        assert int(control[0]) == step_ref == wl.steps
+        for b in range(B):
+            occ = np.nonzero(slot_ref[b] >= 0)[0]
+            np.testing.assert_array_equal(buf[b].cpu().numpy()[occ], h.export_buffer(b)[occ])
+    finally:
+        ref.close()
+
+
 def test_parity_two_thousand_steps():
     """A long run: slots that go unused for more than 1023 steps leave the
     exact-age bins, so the victim search takes its radix-select path in the
