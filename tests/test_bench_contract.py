@@ -30,3 +30,24 @@ def test_warmup_below_three_is_refused():
                         "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
                        timeout=120, cwd=ROOT)
     assert r.returncode != 0
+
+
+def test_oracle_legs_replay_every_layer_with_appends():
+    """The CPU legs time every layer of the sample and a growing context's
+    appends: their state after the run equals a direct oracle replay."""
+    import types
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from hierarchical_kv_cache_hs_gb300 import tracegen as tg
+    wl = tg.Workload("legs", 77, B=3, C=600, K=40, S=80, T=16, host_ratio=8, layers=2, steps=30,
+                     len0=584, grow=1, carry_pct=60, zipf_pct=30, third=tg.THIRD_RECENT, recent=64)
+    assert bench._oracle_sample(wl) == [0, 1, 2]
+    line = bench.cpu_baseline(wl, types.SimpleNamespace(warmup=3, steps=8), bench.PRIME_STEPS + 11)
+    assert line["value"] > 0 and "2 layers" in line["sample"] and "appended" in line["sample"]
+    # the big 4-layer workload is sampled to fit the host-memory bound
+    big = tg.WORKLOADS["b64_c128k_l4_tail4096"]
+    n = len(bench._oracle_sample(big))
+    assert 1 <= n < big.B
+    assert n * big.layers * big.cold * big.row_bytes <= bench.ORACLE_HOST_BYTES
