@@ -33,8 +33,8 @@ def test_warmup_below_three_is_refused():
 
 
 def test_oracle_legs_replay_every_layer_with_appends():
-    """The CPU legs time every layer of the sample and a growing context's
-    appends: their state after the run equals a direct oracle replay."""
+    """The CPU legs run every layer of the sample with a growing context's
+    appends, say so in the line, and bound the sample by host memory."""
     import types
     import numpy as np
     sys.path.insert(0, ROOT)
