@@ -323,6 +323,47 @@ def test_noalloc_random_matches_handle_path(seed):
         ref.close()
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_parity_random_entry_points(seed):
+    """Random workloads through the other entry points: the whole run replayed
+    from one CUDA graph, the copy-engine variant, or host buffers (against the
+    device path step by step)."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _random_workload(400 + seed)
+    rng = random.Random(3000 + seed)
+    one = wl.layers > 1 and rng.random() < 0.5
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    kind = seed % 3
+    if kind < 2:
+        res = gpu_run(wl, graph=kind == 0, copy_engine=kind == 1, one_launch=one and kind == 0,
+                      copy_mode=rng.choice([0, 1, 2]))
+        try:
+            tot, err = compare(wl, res)
+            check_counters(wl, res, tot, err | expect)
+        finally:
+            res.workload.close()
+        return
+    a = GpuWorkload(wl, record=True)
+    b = GpuWorkload(wl, record=False, host_trace=True)
+    try:
+        out_host = torch.empty((wl.layers, wl.B, wl.K), dtype=torch.int32).pin_memory()
+        for s in range(wl.steps):
+            a.launch_step(s, one_launch=one)
+            b.host_step(s, out_host, one_launch=one)
+            torch.cuda.synchronize()
+            assert torch.equal(a.out[:, s].cpu(), out_host), s
+        for ha, hb in zip(a.handles, b.handles):
+            for x, y in zip(ha.export_state(), hb.export_state()):
+                np.testing.assert_array_equal(x, y)
+            assert ha.stats()["misses"] == hb.stats()["misses"]
+    finally:
+        a.close()
+        b.close()
+
+
 def test_parity_two_thousand_steps():
     """A long run: slots that go unused for more than 1023 steps leave the
     exact-age bins, so the victim search takes its radix-select path in the
