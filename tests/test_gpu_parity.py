@@ -364,6 +364,36 @@ def test_parity_random_entry_points(seed):
         b.close()
 
 
+def test_handles_driven_from_two_host_threads():
+    """Two handles, each created and stepped from its own host thread on its
+    own stream at the same time; both match the oracle."""
+    import threading
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wls = [_random_workload(900), _random_workload(901)]
+    results, errors = [None, None], []
+
+    def run(i):
+        try:
+            results[i] = gpu_run(wls[i], copy_mode=i + 1)  # each run makes its own stream
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for wl, res in zip(wls, results):
+        try:
+            tot, err = compare(wl, res)
+            expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+            check_counters(wl, res, tot, err | expect)
+        finally:
+            res.workload.close()
+
+
 def test_parity_two_thousand_steps():
     """A long run: slots that go unused for more than 1023 steps leave the
     exact-age bins, so the victim search takes its radix-select path in the
