@@ -28,9 +28,9 @@
 //   FUSED   the CTA then updates the tables and copies its own missing rows
 //           from the mapped host pool into the buffer (zero-copy 128-bit
 //           loads, U in flight per lane); the last CTA to finish advances the
-//           step counter.  One launch per step.  Each warp loads its first
-//           row group into registers as soon as the miss list exists, so the
-//           host link is busy while the victims are chosen.  (Staging those
+//           step counter.  One launch per step.  Half of the warps load
+//           their first row group into registers as soon as the miss list
+//           exists, so the host link is busy while the victims are chosen.  (Staging those
 //           rows in shared memory instead -- cp.async, or bulk copies on an
 //           mbarrier issued by a separate fetch warp -- was measured no
 //           faster.)
