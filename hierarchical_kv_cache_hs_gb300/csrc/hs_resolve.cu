@@ -30,10 +30,10 @@
 //           loads, U in flight per lane); the last CTA to finish advances the
 //           step counter.  One launch per step.  Half of the warps load
 //           their first row group into registers as soon as the miss list
-//           exists, so the host link is busy while the victims are chosen.  (Staging those
-//           rows in shared memory instead -- cp.async, or bulk copies on an
-//           mbarrier issued by a separate fetch warp -- was measured no
-//           faster.)
+//           exists, so the host link is busy while the victims are chosen.
+//           (Staging rows in shared memory instead -- cp.async, or bulk
+//           copies on mbarriers issued by a separate fetch warp -- was
+//           measured no faster.)
 //   !FUSED  the CTA writes the miss / victim lists to global memory for the
 //           grid-wide copy kernel (hs_copy.cu), which advances the counter.
 //
