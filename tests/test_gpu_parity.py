@@ -142,7 +142,8 @@ def _random_workload(seed):
     ratio = -(-(C - T) // S)  # enough host rows for the cold tokens
     steps = rng.randint(5, 40)
     if sliding:
-        len0 = rng.randint(min(T, C - 8), C - 8)  # the tail holds the last T tokens written
+        # the tail holds the last T tokens written; the first row needs K tokens
+        len0 = rng.randint(max(min(T, C - 8), K), C - 8)
         steps = min(steps, C - len0)
     else:
         len0 = C - T if grow else C  # a fixed tail starts empty when the context grows
