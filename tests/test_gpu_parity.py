@@ -414,6 +414,21 @@ def test_create_accepts_a_pool_that_covers_the_cold_tokens():
     hs.hs_destroy(h)
 
 
+def test_one_launch_at_the_layer_limit():
+    """HS_MAX_LAYERS (16) handles in one launch, against the oracle."""
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = tg.Workload("layers16", 76, B=5, C=3000, K=200, S=400, T=64, host_ratio=8,
+                     layers=hs.HS_MAX_LAYERS, steps=12, len0=3000, grow=0, carry_pct=60,
+                     zipf_pct=30, third=tg.THIRD_ZIPF)
+    res = gpu_run(wl, one_launch=True, policy=[l % 2 for l in range(wl.layers)])
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+    finally:
+        res.workload.close()
+
+
 def test_one_launch_argument_checks():
     from hierarchical_kv_cache_hs_gb300 import hs
     a = hs.Handle(4, 2048, 64, 256, 8)
