@@ -157,6 +157,67 @@ def _random_workload(seed):
                        sliding=sliding)
 
 
+def _wide_workload(seed):
+    """Random sizes up to the kernel limits: S to 16384, K to 4096, rows to 64 KB."""
+    import random
+    rng = random.Random(seed)
+    S = rng.choice([1, 2, 3, 5, 33, 127, 1000, 4095, 4096, 8191, 16384])
+    K = rng.randint(1, min(S, 4096))
+    if rng.random() < 0.2:
+        K = min(S, 4096)
+    T = rng.choice([0, 0, 1, 3, 64, 1000])
+    grow = T > 0 and rng.random() < 0.5
+    sliding = grow and rng.random() < 0.5
+    R = 16 * rng.choice([1, 2, 3, 65, 72, 129, 256, 1024, 4096])
+    B = rng.choice([1, 2, 16, 17, 64, 150])
+    layers = rng.choice([1, 1, 2])
+    C = rng.randint(max(K, 8), max(K, 8) + rng.choice([10, 1000, 30000])) + T
+    # keep the pinned pools under ~3 GB and the device buffers under ~2 GB
+    while layers * B * C * R > 3e9 or layers * B * (S + T) * R > 2e9:
+        if B > 1:
+            B = max(1, B // 2)
+        elif layers > 1:
+            layers = 1
+        else:
+            R = 16
+            break
+    ratio = -(-(C - T) // S)
+    steps = rng.randint(3, 25)
+    if sliding and max(min(T, C - 8), K) > C - 8:
+        sliding = False
+    if sliding:
+        len0 = rng.randint(max(min(T, C - 8), K), C - 8)
+        steps = min(steps, C - len0)
+    else:
+        len0 = C - T if grow else C
+    carry = rng.choice([0, 50, 90])
+    return tg.Workload("wide%d" % seed, 40 + seed % 30, B=B, C=C, K=K, S=S, T=T, host_ratio=ratio,
+                       layers=layers, steps=steps, len0=len0, grow=1 if grow else 0,
+                       carry_pct=carry, zipf_pct=rng.choice([0, 100 - carry - 5]),
+                       third=rng.choice([tg.THIRD_ZIPF, tg.THIRD_UNIFORM]), row_bytes=R, sliding=sliding)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_parity_wide_random(seed):
+    """Seeded random workloads drawn up to the kernel limits, every request of
+    every layer against the oracle."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _wide_workload(seed)
+    rng = random.Random(9000 + seed)
+    mode = rng.choice([0, 1, 2])
+    pol = [rng.choice([0, 1]) for _ in range(wl.layers)]
+    one = wl.layers > 1 and rng.random() < 0.5
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, copy_mode=mode, policy=pol, one_launch=one)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+    finally:
+        res.workload.close()
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_parity_random_multi_position(seed):
     """Seeded random draft-position steps: P rows per request that repeat one
