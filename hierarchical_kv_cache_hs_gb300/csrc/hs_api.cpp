@@ -436,13 +436,21 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
         if (ok) h->ce_h_cnt = static_cast<int32_t*>(p);
         ok = ok && cudaHostAlloc(&p, B * S * sizeof(int32_t), cudaHostAllocDefault) == cudaSuccess;
         if (ok) h->ce_h_tok = static_cast<int32_t*>(p);
-        if (!ok) {
+        unsigned n = std::thread::hardware_concurrency();
+        if (ok) h->ce_pool = new (std::nothrow) GatherPool(n ? (int)n : 4);
+        if (!ok || !h->ce_pool) {
+            // Release what was allocated so that a later call starts afresh.
             cudaGetLastError();
+            if (h->ce_h_stage) cudaFreeHost(h->ce_h_stage);
+            if (h->ce_d_stage) cudaFree(h->ce_d_stage);
+            if (h->ce_h_cnt) cudaFreeHost(h->ce_h_cnt);
+            if (h->ce_h_tok) cudaFreeHost(h->ce_h_tok);
+            h->ce_h_stage = nullptr;
+            h->ce_d_stage = nullptr;
+            h->ce_h_cnt = nullptr;
+            h->ce_h_tok = nullptr;
             return HS_ERR_ALLOC;
         }
-        unsigned n = std::thread::hardware_concurrency();
-        h->ce_pool = new (std::nothrow) GatherPool(n ? (int)n : 4);
-        if (!h->ce_pool) return HS_ERR_ALLOC;
     }
 
     // (1)-(3) on the device: the resolve kernel writes the miss lists.
