@@ -428,10 +428,13 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
     const size_t B = (size_t)h->B, S = (size_t)h->S, R = (size_t)h->R;
     if (!h->ce_pool) {
         const size_t rows = B * (size_t)(h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK);
+        // Each pointer is stored only once its allocation has succeeded, so the
+        // error path below frees exactly what exists.
         void* p = nullptr;
         bool ok = cudaHostAlloc(&p, rows * R, cudaHostAllocDefault) == cudaSuccess;
-        h->ce_h_stage = static_cast<uint8_t*>(p);
-        ok = ok && cudaMalloc(reinterpret_cast<void**>(&h->ce_d_stage), rows * R) == cudaSuccess;
+        if (ok) h->ce_h_stage = static_cast<uint8_t*>(p);
+        ok = ok && cudaMalloc(&p, rows * R) == cudaSuccess;
+        if (ok) h->ce_d_stage = static_cast<uint8_t*>(p);
         ok = ok && cudaHostAlloc(&p, B * sizeof(int32_t), cudaHostAllocDefault) == cudaSuccess;
         if (ok) h->ce_h_cnt = static_cast<int32_t*>(p);
         ok = ok && cudaHostAlloc(&p, B * S * sizeof(int32_t), cudaHostAllocDefault) == cudaSuccess;
