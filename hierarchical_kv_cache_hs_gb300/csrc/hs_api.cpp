@@ -186,8 +186,8 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     if (ok) {
         void* p = nullptr;
         ok = cudaHostAlloc(&p, h->pool_bytes ? h->pool_bytes : 1, cudaHostAllocMapped) == cudaSuccess;
-        h->h_pool = static_cast<uint8_t*>(p);
         if (ok) {
+            h->h_pool = static_cast<uint8_t*>(p);
             void* dp = nullptr;
             ok = cudaHostGetDevicePointer(&dp, p, 0) == cudaSuccess;
             h->d_pool = static_cast<uint8_t*>(dp);
@@ -491,7 +491,12 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
         cudaStreamSynchronize(s) != cudaSuccess)
         return HS_ERR_CUDA;
     std::vector<long long> off(B + 1, 0);
-    for (size_t b = 0; b < B; ++b) off[b + 1] = off[b] + h->ce_h_cnt[b];
+    // A request's misses never exceed K, which the staging area is sized for;
+    // the clamp keeps the host gather inside it whatever the device wrote.
+    for (size_t b = 0; b < B; ++b) {
+        const int32_t c = h->ce_h_cnt[b];
+        off[b + 1] = off[b] + (c < 0 ? 0 : c > K ? K : c);
+    }
     const long long M = off[B];
 
     // Host threads gather the rows into the staging area in flattened
@@ -511,6 +516,7 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
             while (off[b + 1] <= r) ++b;
             const long long i = r - off[b];
             const int32_t t = toks[b * S + (size_t)i];
+            if (t < 0 || t >= H) continue;  // never written by the resolve kernel
             std::memcpy(stage + (size_t)r * R, pool + ((long long)b * H + t) * (long long)R, R);
         }
     };
