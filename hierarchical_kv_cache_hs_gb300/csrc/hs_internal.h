@@ -94,28 +94,39 @@ constexpr int HS_COPY_THREADS = 256;
 constexpr int HS_AGE_BINS = 1024;
 constexpr int HS_AGE_SUBHIST = 4;
 
-// Ints of the region shared by the dedup hash (2 << hash_bits) and the age
-// histograms (HS_AGE_SUBHIST * HS_AGE_BINS).
-__host__ __device__ inline int hs_resolve_region_a_ints(int hash_bits)
+// Bits of the dedup hash: at least 2K entries, so it is at most half full.
+__host__ __device__ inline int hs_hash_bits(int K)
 {
-    const int hc2 = 2 << hash_bits;
-    const int hist = HS_AGE_SUBHIST * HS_AGE_BINS;
-    return hc2 > hist ? hc2 : hist;
+    int bits = 6;
+    while ((1 << bits) < 2 * K) ++bits;
+    return bits;
 }
 
-// Shared memory of the resolve kernel: region A, stamps [S], slot -> token
+// Ints of the region shared by the dedup hash (2 << hash_bits) in phase 1 and,
+// once the miss list exists, the age histograms (HS_AGE_SUBHIST * HS_AGE_BINS)
+// followed by the K-entry out_slot row.  With K >= 1366 the hash alone is
+// larger than both.  A multiple of 4 ints, so that the stamp row after it
+// starts on the 16-byte boundary its asynchronous copies and int4 reads need.
+__host__ __device__ inline int hs_resolve_region_a_ints(int hash_bits, int K)
+{
+    const int hc2 = 2 << hash_bits;
+    const int later = (HS_AGE_SUBHIST * HS_AGE_BINS + K + 3) & ~3;
+    return hc2 > later ? hc2 : later;
+}
+
+// Shared memory of the resolve kernel: region A (hash; then histograms and
+// the out_slot row), stamps [S], slot -> token
 // [S], miss tokens [K] (ints); miss row positions [K], victims [K] (uint16);
 // the hit bitmap [ceil(S/32)] (words).
 __host__ __device__ inline size_t hs_resolve_base_bytes(int K, int S, int hash_bits)
 {
-    const size_t ints = (size_t)hs_resolve_region_a_ints(hash_bits) + 2u * (size_t)S + (size_t)K;
+    const size_t ints = (size_t)hs_resolve_region_a_ints(hash_bits, K) + 2u * (size_t)S + (size_t)K;
     size_t bytes = 4u * ints + 2u * 2u * (size_t)K;
     bytes += 4u * (size_t)((S + 31) >> 5);
     return bytes;
 }
 
 size_t hs_resolve_smem_bytes(int K, int S);
-int hs_hash_bits(int K);
 cudaError_t hs_prepare_resolve();
 // Resolve only: writes the miss lists for hs_launch_copy.
 cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s);

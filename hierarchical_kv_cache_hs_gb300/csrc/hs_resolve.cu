@@ -11,7 +11,11 @@
 //     repeated indices (the first occurrence wins), built while the
 //     page-table gathers are in flight;
 //   - the miss list in top-k row order (block scan of per-thread counts);
-//   - the victim list in ascending slot order.
+//   - the victim list in ascending slot order;
+//   - the out_slot row, kept until the victims are known and then written
+//     once, each thread's contiguous entries as 16-byte stores (out_slot may
+//     be mapped host memory, where scattered 4-byte writes slowed the step
+//     by 6 %).
 //
 // Victims are the m slots with the smallest (stamp, slot) pairs.  One
 // 1024-bin histogram of stamp ages (step - stamp, ages >= 1023 share the
@@ -148,6 +152,30 @@ __device__ __forceinline__ int clamp_stamp(int k, int step)
     return k < 0 ? 0 : (k >= step ? step - 1 : k);
 }
 
+// One thread's out_slot entries [j0, j0 + E) that lie below K, written with
+// 16-byte (else 8-byte) stores where the run is whole and aligned.  A warp's
+// stores then cover whole lines: out_slot may be mapped host memory, where
+// scattered 4-byte writes each take a transaction on the host link.
+__device__ __forceinline__ void write_out(int32_t* g_out, const int (&o)[EMAX], int j0, int E,
+                                          int K)
+{
+    int32_t* dst = g_out + j0;
+    const int n = j0 + E <= K ? E : (K > j0 ? K - j0 : 0);
+    if (n == E && (E & 3) == 0 && ((uintptr_t)dst & 15u) == 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; e += 4)
+            if (e < E) *reinterpret_cast<int4*>(dst + e) = make_int4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+    } else if (n == E && (E & 1) == 0 && ((uintptr_t)dst & 7u) == 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; e += 2)
+            if (e < E) *reinterpret_cast<int2*>(dst + e) = make_int2(o[e], o[e + 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if (e < n) dst[e] = o[e];
+    }
+}
+
 // One request's step: CTA `b` of the `nblocks` that serve one handle.
 template <bool FUSED, int U>
 __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
@@ -166,10 +194,11 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
 
     const int K = a.K, S = a.S;
     const int hc = 1 << a.hash_bits;
-    const int region_a = hs_resolve_region_a_ints(a.hash_bits);
+    const int region_a = hs_resolve_region_a_ints(a.hash_bits, K);
     int* s_hkey = smem;                       // [hc]   phase 1
     int* s_hj = smem + hc;                    // [hc]   phase 1
     int* s_hist = smem;                       // [NSUB][NB], phase 2 (reuses the hash)
+    int* s_out = smem + NSUB * NB;            // [K]    after the miss list (reuses the hash)
     int* s_stamp = smem + region_a;           // [S]
     int* s_slot_tok = s_stamp + S;            // [S]
     int* s_mtok = s_slot_tok + S;             // [K]
@@ -211,7 +240,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     // copies when they are 16-byte aligned, so all of them are in flight at
     // once; otherwise with plain loads.
     const bool vec_rows = (S & 3) == 0 &&
-        (((uintptr_t)g_stamp | (uintptr_t)g_slot_tok) & 15u) == 0;
+        (((uintptr_t)g_stamp | (uintptr_t)g_slot_tok | (uintptr_t)s_stamp) & 15u) == 0;
     if (vec_rows) {
         for (int i = tid; i < (S >> 2); i += NT) {
             cp_async16(s_stamp + 4 * i, g_stamp + 4 * i);
@@ -234,6 +263,11 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     // The page-table gathers are issued before waiting for the stamp rows, so
     // their DRAM latency overlaps the wait.
     int cl[EMAX], hs[EMAX], sl[EMAX];
+    // out_slot values of the thread's entries, written to memory once per
+    // step (write_out below).  A miss holds -(2 + its miss index) until its
+    // victim is known; under aliasing a repeated miss holds
+    // -(2 + K + row of its first occurrence).
+    int ov[EMAX];
     int err = 0;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
@@ -319,10 +353,10 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 if (s_stamp[sl[e]] != step + (K - j)) {
                     cl[e] = C_BAD;
                     if (a.alias) {
-                        g_out[j] = sl[e];  // the same resident slot as its first occurrence
+                        ov[e] = sl[e];  // the same resident slot as its first occurrence
                     } else {
                         err |= HS_E_DUP;
-                        g_out[j] = -1;
+                        ov[e] = -1;
                     }
                 } else {
                     cl[e] = C_HIT;
@@ -331,30 +365,29 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                     // kept at write-back.
                     s_stamp[sl[e]] = step;
                     if (a.fifo) atomicOr(&s_hitbits[sl[e] >> 5], 1u << (sl[e] & 31));
-                    g_out[j] = sl[e];
+                    ov[e] = sl[e];
                     ++nh;
                 }
             } else if (s_hj[hs[e]] != j) {
                 cl[e] = C_BAD;
                 if (!a.alias) {
                     err |= HS_E_DUP;
-                    g_out[j] = -1;
+                    ov[e] = -1;
                 } else if (tk[e] >= cold) {
-                    g_out[j] = S + tk[e] % a.T;
+                    ov[e] = S + tk[e] % a.T;
                 } else {
-                    // A repeated miss: its slot is known only after the
-                    // pairing.  Leave -(first + 2) and resolve it at the end.
-                    g_out[j] = -(s_hj[hs[e]] + 2);
+                    // A repeated miss takes its first occurrence's slot.
+                    ov[e] = -(2 + K + s_hj[hs[e]]);
                 }
             } else if (tk[e] >= cold) {
                 cl[e] = C_TAIL;
-                g_out[j] = S + tk[e] % a.T;
+                ov[e] = S + tk[e] % a.T;
                 ++ni;
             } else {
                 ++nm;
             }
-        } else if (e < E && j < K) {
-            g_out[j] = -1;
+        } else {
+            ov[e] = -1;
         }
     }
     nh = __reduce_add_sync(FULL, nh);
@@ -373,11 +406,20 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         if (cl[e] == C_MISS) {
             s_mtok[pos] = tk[e];
             s_mj[pos] = (uint16_t)(j0 + e);
+            ov[e] = -(2 + pos);
             ++pos;
         }
     }
 
-    if (m > 0) {
+    if (m == 0) {
+        write_out(g_out, ov, j0, E, K);
+    } else {
+        // The hash is no longer read (the scan above passed a barrier), so
+        // its region keeps the thread's out values through phase 2.
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if (e < E && j0 + e < K) s_out[j0 + e] = ov[e];
+
         // ---- (2) LRU victims ----------------------------------------------
         // Age histogram: bin NB-1-min(age, NB-1), so older slots sit in lower
         // bins and the shared bin 0 holds every age >= NB-1.
@@ -502,7 +544,8 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         const int Q = (S + NT - 1) / NT;
         const int q0 = tid * Q;
         int nl = 0, ne = 0;
-        const bool vec_q = (Q & 3) == 0 && q0 + Q <= S;  // 16-byte aligned, all in range
+        const bool vec_q = (Q & 3) == 0 && q0 + Q <= S &&  // 16-byte aligned, all in range
+                           ((uintptr_t)s_stamp & 15u) == 0;
         if (vec_q) {
             for (int q = 0; q < Q; q += 4) {
                 const int4 k4 = *reinterpret_cast<const int4*>(s_stamp + q0 + q);
@@ -552,6 +595,34 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         }
         __syncthreads();
 
+        // The i-th miss (row order) is paired with the i-th victim, so every
+        // out value is known now: one write of the thread's entries.
+        {
+            int fo[EMAX];
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                int o = (e < E && j0 + e < K) ? s_out[j0 + e] : -1;
+                if (o <= -2) {
+                    int i = -o - 2;
+                    if (i >= K) {
+                        // first occurrence at row i - K: find its miss index
+                        // (the miss rows are ascending)
+                        const int jf = i - K;
+                        int lo = 0, hi = m;
+                        while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            if ((int)s_mj[mid] < jf) lo = mid + 1;
+                            else hi = mid;
+                        }
+                        i = lo;
+                    }
+                    o = i < m ? (int)s_vic[i] : -1;
+                }
+                fo[e] = o;
+            }
+            write_out(g_out, fo, j0, E, K);
+        }
+
         if (!FUSED) {
             // ---- (3) pair the i-th miss (row order) with the i-th victim ----
             int32_t* g_mtok = a.miss_tok + (size_t)b * a.list_stride;
@@ -567,7 +638,6 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 g_slot_tok[v] = t;
                 g_tok_slot[t] = v;
                 s_stamp[v] = step;
-                g_out[s_mj[i]] = v;
                 g_mtok[i] = t;
                 g_mslot[i] = v;
             }
@@ -589,7 +659,6 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                     g_slot_tok[v] = t;
                     g_tok_slot[t] = v;
                     s_stamp[v] = step;
-                    g_out[s_mj[i]] = v;
                     src = (long long)t * a.R;
                     dst = (long long)v * a.R;
                 }
@@ -611,17 +680,6 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         }
     }
     __syncthreads();
-    if (a.alias && m > 0) {
-        // Repeated misses take the slot their first occurrence was paired with
-        // (written to out_slot above, before the barrier).
-        for (int e = 0; e < EMAX; ++e) {
-            const int j = j0 + e;
-            if (e < E && j < K) {
-                const int o = g_out[j];
-                if (o <= -2) g_out[j] = g_out[-o - 2];
-            }
-        }
-    }
     if (a.fifo) {
         for (int i = tid; i < S; i += NT)
             if (!((s_hitbits[i >> 5] >> (i & 31)) & 1u)) g_stamp[i] = s_stamp[i];
@@ -665,13 +723,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_layers_kernel(const __grid_c
 
 }  // namespace
 
-int hs_hash_bits(int K)
-{
-    int bits = 6;
-    while ((1 << bits) < 2 * K) ++bits;
-    return bits;
-}
-
 size_t hs_resolve_smem_bytes(int K, int S)
 {
     return hs_resolve_base_bytes(K, S, hs_hash_bits(K));
@@ -697,8 +748,16 @@ cudaError_t hs_prepare_resolve()
     return e;
 }
 
+// The kernel places its stamp row right after region A and copies into it
+// with 16-byte asynchronous copies: refuse a layout that would misalign it.
+static bool layout_ok(const ResolveArgs& a)
+{
+    return a.hash_bits == hs_hash_bits(a.K) && (hs_resolve_region_a_ints(a.hash_bits, a.K) & 3) == 0;
+}
+
 cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s)
 {
+    if (!layout_ok(a)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(NT);
@@ -709,6 +768,7 @@ cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s)
 
 cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream_t s)
 {
+    if (!layout_ok(a)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(NT);
@@ -720,6 +780,8 @@ cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream
 
 cudaError_t hs_launch_swapin_layers(const LayerArgs& p, int L, int unroll, cudaStream_t s)
 {
+    for (int l = 0; l < L; ++l)
+        if (!layout_ok(p.l[l])) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(L * p.B));
     cfg.blockDim = dim3(NT);
