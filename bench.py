@@ -386,20 +386,30 @@ def run_ours(args, rank, world, dist):
                     hs.hs_set_policy(h.h, pol)
                 import numpy as np
                 last = np.zeros(wl.B, dtype=np.int32)
-                ms, per_step = 0.0, []
+                per_step = []
+                e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+                e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
                 with torch.cuda.stream(stream):
+                    # Timed pass: launches queued ahead as in the main pass, so no
+                    # host round trip falls inside a step's events.
                     for s in range(PRIME_STEPS + args.warmup):
                         w.launch_step(s, stream)
                     for i in range(args.steps):
                         s = PRIME_STEPS + args.warmup + i
                         flush.fill_(i & 0xFF)
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
+                        e0[i].record(stream)
                         w.launch_step(s, stream)
-                        e1.record(stream)
-                        e1.synchronize()
-                        ms += e0.elapsed_time(e1)
+                        e1[i].record(stream)
+                    stream.synchronize()
+                    ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
+                    # Counting pass over the same steps: per-step miss counts.
+                    w.reset()
+                    for h in w.handles:
+                        hs.hs_set_policy(h.h, pol)
+                    for s in range(PRIME_STEPS + args.warmup):
+                        w.launch_step(s, stream)
+                    for i in range(args.steps):
+                        w.launch_step(PRIME_STEPS + args.warmup + i, stream)
                         tot = 0
                         for h in w.handles:
                             hs.hs_stats(h.h, last)
