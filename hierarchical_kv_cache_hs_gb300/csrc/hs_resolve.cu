@@ -198,7 +198,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     int* s_hkey = smem;                       // [hc]   phase 1
     int* s_hj = smem + hc;                    // [hc]   phase 1
     int* s_hist = smem;                       // [NSUB][NB], phase 2 (reuses the hash)
-    int* s_out = smem + NSUB * NB;            // [K]    after the miss list (reuses the hash)
+    int* s_out = smem + NSUB * NB;            // [E][NT] after the miss list (reuses the hash)
     int* s_stamp = smem + region_a;           // [S]
     int* s_slot_tok = s_stamp + S;            // [S]
     int* s_mtok = s_slot_tok + S;             // [K]
@@ -415,10 +415,11 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         write_out(g_out, ov, j0, E, K);
     } else {
         // The hash is no longer read (the scan above passed a barrier), so
-        // its region keeps the thread's out values through phase 2.
+        // its region keeps the thread's out values through phase 2, entry e
+        // at e * NT + tid: a warp's accesses hit 32 different banks.
 #pragma unroll
         for (int e = 0; e < EMAX; ++e)
-            if (e < E && j0 + e < K) s_out[j0 + e] = ov[e];
+            if (e < E) s_out[e * NT + tid] = ov[e];
 
         // ---- (2) LRU victims ----------------------------------------------
         // Age histogram: bin NB-1-min(age, NB-1), so older slots sit in lower
@@ -601,7 +602,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             int fo[EMAX];
 #pragma unroll
             for (int e = 0; e < EMAX; ++e) {
-                int o = (e < E && j0 + e < K) ? s_out[j0 + e] : -1;
+                int o = e < E ? s_out[e * NT + tid] : -1;
                 if (o <= -2) {
                     int i = -o - 2;
                     if (i >= K) {

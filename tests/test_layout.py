@@ -29,8 +29,9 @@ int main()
         if ((1 << bits) < 2 * K) { printf("K=%d: hash more than half full\n", K); return 1; }
         if (A % 4 != 0) { printf("K=%d: region A of %d ints misaligns the stamp row\n", K, A); return 1; }
         if (A < (2 << bits)) { printf("K=%d: region A smaller than the hash\n", K); return 1; }
-        if (A < HS_AGE_SUBHIST * HS_AGE_BINS + K) {
-            printf("K=%d: region A smaller than histograms + out row\n", K);
+        const int E = (K + HS_RESOLVE_THREADS - 1) / HS_RESOLVE_THREADS;
+        if (A < HS_AGE_SUBHIST * HS_AGE_BINS + E * HS_RESOLVE_THREADS) {
+            printf("K=%d: region A smaller than histograms + out values\n", K);
             return 1;
         }
         const int Ss[] = {K, K + 1, K + 2, K + 3, HS_MAX_SLOTS};
