@@ -433,11 +433,12 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         // waits while the SM's memory path is full, so the other half runs the
         // victim search unhindered (measured: all 16 warps 1.8 % faster per
         // step than none; 8 warps a further 1.8 % faster at 32 requests and no
-        // slower at 64 or 256).
+        // slower at 64 or 256).  When one round of the copy loop takes every
+        // row (m <= NW * G0) the early loads only delay the victim search.
         uint4 pre[U];
         const int G0 = a.rows_per_group;
         const int cpr0 = a.R >> 4;
-        const bool prefetch = FUSED && G0 * cpr0 <= 32 * U && warp < NW / 2;
+        const bool prefetch = FUSED && G0 * cpr0 <= 32 * U && warp < NW / 2 && m > NW * G0;
         if (prefetch && warp * G0 < m) {
             const uint8_t* pool_b0 = a.pool + (size_t)b * (size_t)a.H * a.R;
             const int r0 = warp * G0;
