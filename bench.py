@@ -40,11 +40,11 @@ PRIME_STEPS = 10
 # fused swap-in kernel on the 64-request, 64K-context, 4096-slot workload, from
 # its ncu capture (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md).  The
 # host-link bytes equal the algorithmic miss-row bytes of that launch.
-FUSED_NCU_DRAM_BYTES = 9071360 + 722688
+FUSED_NCU_DRAM_BYTES = 9070848 + 779008
 FUSED_NCU_SYSMEM_BYTES = 933264 * 32
 # The same for the one-launch layers kernel on the 4-layer, 64-request,
 # 128K-context workload (profiles/hs_resolve_layers_kernel_b64_c128k_l4.md).
-LAYERS_NCU_DRAM_BYTES = 45484800 + 66257152
+LAYERS_NCU_DRAM_BYTES = 45681408 + 66817024
 LAYERS_NCU_SYSMEM_BYTES = 3410100 * 32
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20
