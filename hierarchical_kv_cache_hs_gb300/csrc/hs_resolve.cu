@@ -34,7 +34,8 @@
 //           loads, U in flight per lane); the last CTA to finish advances the
 //           step counter.  One launch per step.  Half of the warps load
 //           their first row group into registers as soon as the miss list
-//           exists, so the host link is busy while the victims are chosen.
+//           exists, so the host link is busy while the victims are chosen
+//           (unless one round of the copy loop takes every row).
 //           (Staging rows in shared memory instead -- cp.async, or bulk
 //           copies on mbarriers issued by a separate fetch warp -- was
 //           measured no faster.)
