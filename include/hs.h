@@ -186,7 +186,10 @@ int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* cons
  * are page-locked and mapped into the device address space (cudaHostAlloc,
  * cudaMallocHost, or cudaHostRegister with mapping), the kernels read and
  * write them across the host link directly; otherwise they are staged
- * through device buffers with two cudaMemcpyAsync.  Not graph-capturable
+ * through device buffers with two cudaMemcpyAsync.  The choice follows
+ * cudaHostGetDevicePointer: on a system whose GPU addresses pageable host
+ * memory (a Grace host), it can accept ordinary malloc'd buffers too, and
+ * those are then read and written in place as well.  Not graph-capturable
  * (it synchronises).
  */
 int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
