@@ -121,6 +121,15 @@ bool valid(const hs_handle* h)
     return h != nullptr && h->B > 0;
 }
 
+// The launch mode of a step (HS_COPY_AUTO: by batch size, or by the size of
+// one request's hot buffer, which bounds what a step gives one CTA to copy).
+bool use_fused(const hs_handle* h)
+{
+    if (h->copy_mode != HS_COPY_AUTO) return h->copy_mode == HS_COPY_FUSED;
+    return h->B >= HS_FUSED_MIN_BATCH ||
+           (long long)h->S * h->R <= (long long)HS_FUSED_MAX_REQUEST_BYTES;
+}
+
 }  // namespace
 
 extern "C" {
@@ -297,8 +306,7 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     const ResolveArgs ra = resolve_args(h, topk_idx, K, out_slot, alias);
 
     const bool prof = h->prof_before && h->prof_after;
-    const bool fused = h->copy_mode == HS_COPY_FUSED ||
-                       (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
+    const bool fused = use_fused(h);
     if (fused) {
         // One launch: each request's CTA fetches its own rows.  The profiling
         // events then bracket the whole step.
@@ -549,8 +557,7 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
 int hs_resolve_launches(hs_handle* h)
 {
     if (!valid(h)) return HS_ERR_ARG;
-    const bool fused = h->copy_mode == HS_COPY_FUSED ||
-                       (h->copy_mode == HS_COPY_AUTO && h->B >= HS_FUSED_MIN_BATCH);
+    const bool fused = use_fused(h);
     return fused ? 1 : 2;
 }
 

@@ -42,6 +42,7 @@ HS_COPY_AUTO = 0
 HS_COPY_FUSED = 1
 HS_COPY_SPLIT = 2
 HS_FUSED_MIN_BATCH = 16
+HS_FUSED_MAX_REQUEST_BYTES = 1 << 20
 
 HS_MAX_TOPK = 4096
 HS_MAX_SLOTS = 16384

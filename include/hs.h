@@ -308,12 +308,17 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
  *                  fetches its own missing rows from the host pool;
  *   HS_COPY_SPLIT  a resolve kernel, then a grid-wide copy kernel over the
  *                  misses of all requests (better when B is small);
- *   HS_COPY_AUTO   fused when B >= HS_FUSED_MIN_BATCH, split otherwise (default).
+ *   HS_COPY_AUTO   fused when B >= HS_FUSED_MIN_BATCH, or when one request's
+ *                  hot buffer (S * row_bytes) is at most
+ *                  HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
+ *                  much to copy; split otherwise (default).  A function of the
+ *                  handle alone, so hs_resolve_launches answers per handle.
  */
 #define HS_COPY_AUTO   0
 #define HS_COPY_FUSED  1
 #define HS_COPY_SPLIT  2
 #define HS_FUSED_MIN_BATCH 16
+#define HS_FUSED_MAX_REQUEST_BYTES (1 << 20)
 int hs_set_copy_mode(hs_handle* h, int mode);
 
 /*
