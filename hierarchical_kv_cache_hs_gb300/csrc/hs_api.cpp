@@ -339,8 +339,11 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     return HS_OK;
 }
 
-int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
-                      int32_t* const* out_slot, hs_stream_t stream)
+// Every host-side check of a several-layer step, shared by the device- and
+// host-buffer entry points so that neither enqueues anything (a staging copy
+// included) for arguments the launch would refuse.
+static int check_layers(hs_handle* const* handles, int L, const void* const* topk_idx, int K,
+                        const void* const* out_slot)
 {
     if (!handles || !topk_idx || !out_slot || L <= 0 || K <= 0) return HS_ERR_ARG;
     if (L > HS_MAX_LAYERS) return HS_ERR_LIMIT;
@@ -356,6 +359,16 @@ int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* to
     }
     if (K > h0->S) return HS_ERR_TOPK_GT_SLOTS;
     if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
+    return HS_OK;
+}
+
+int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
+                      int32_t* const* out_slot, hs_stream_t stream)
+{
+    const int rc = check_layers(handles, L, reinterpret_cast<const void* const*>(topk_idx), K,
+                                reinterpret_cast<const void* const*>(out_slot));
+    if (rc != HS_OK) return rc;
+    const hs_handle* h0 = handles[0];
     DeviceGuard g(h0->device);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -380,14 +393,12 @@ int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* to
 int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
                            int32_t* const* out_slot, hs_stream_t stream)
 {
-    if (!handles || !topk_idx || !out_slot || L <= 0 || K <= 0) return HS_ERR_ARG;
-    if (L > HS_MAX_LAYERS) return HS_ERR_LIMIT;
+    // All checks first: the staging buffers below hold B * min(S, HS_MAX_TOPK)
+    // entries of each handle, which only a checked K and shape respect.
+    const int rc0 = check_layers(handles, L, reinterpret_cast<const void* const*>(topk_idx), K,
+                                 reinterpret_cast<const void* const*>(out_slot));
+    if (rc0 != HS_OK) return rc0;
     const hs_handle* h0 = handles[0];
-    if (!valid(h0)) return HS_ERR_ARG;
-    for (int l = 0; l < L; ++l)
-        if (!valid(handles[l]) || !topk_idx[l] || !out_slot[l]) return HS_ERR_ARG;
-    if (K > h0->S) return HS_ERR_TOPK_GT_SLOTS;
-    if (K > HS_MAX_TOPK) return HS_ERR_LIMIT;
     DeviceGuard g(h0->device);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Device addresses of mapped buffers; the others go through each handle's

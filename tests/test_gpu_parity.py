@@ -812,6 +812,75 @@ def test_layers_host_matches_device_path(pinned):
         b.close()
 
 
+def test_layers_host_refuses_before_staging():
+    """hs_resolve_layers_host with pageable host buffers makes every check of
+    hs_resolve_layers before it stages anything: a second handle with fewer
+    slots (whose staging buffers are smaller than the first handle's K), one
+    with another batch size, a handle given twice and a K beyond the slots
+    each return an error; no handle's state or counters change, the output
+    buffers stay untouched, and the following steps still match the oracle."""
+    from gpu_harness import GpuResult, check_counters, compare
+    from hierarchical_kv_cache_hs_gb300 import hs
+    from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
+    wl = tg.Workload("layers_host_checks", 81, B=4, C=4096, K=400, S=512, T=0, host_ratio=8,
+                     layers=2, steps=8, len0=4096, grow=0, carry_pct=60, zipf_pct=30,
+                     third=tg.THIRD_ZIPF)
+    w = GpuWorkload(wl, record=True)
+    small = hs.Handle(wl.B, wl.C, wl.row_bytes, 256, 16)   # S = 256 < K
+    other_b = hs.Handle(2, wl.C, wl.row_bytes, wl.S, 8)
+    try:
+        stream = torch.cuda.current_stream()
+        L = wl.layers
+        misses = np.zeros((L, wl.steps, wl.B), dtype=np.int32)
+        for s in range(3):
+            w.launch_step(s, stream, one_launch=True)
+            for layer, h in enumerate(w.handles):
+                hs.hs_stats(h.h, misses[layer, s])
+        trace = w.topk.cpu().numpy()            # pageable host memory
+        out = np.full((L, wl.B, wl.K), -7, dtype=np.int32)
+        before = [(h.export_state(), h.stats()) for h in w.handles + [small]]
+        h0, h1 = w.handles[0].h, w.handles[1].h
+        rc = hs.lib.hs_resolve_layers_host
+        P = hs._ptr_array
+
+        def call(handles, K=wl.K):
+            return rc(P(handles), len(handles), P([trace[0, 3]] * len(handles)), K,
+                      P([out[0]] * len(handles)), None)
+
+        assert call([h0, small.h]) == hs.HS_ERR_ARG
+        assert call([small.h, h0]) == hs.HS_ERR_ARG
+        assert call([small.h]) == hs.HS_ERR_TOPK_GT_SLOTS
+        assert call([h0, other_b.h]) == hs.HS_ERR_ARG
+        assert call([h0, h1, h0]) == hs.HS_ERR_ARG
+        assert call([h0, h1], K=wl.S + 1) == hs.HS_ERR_TOPK_GT_SLOTS
+        torch.cuda.synchronize()
+        assert (out == -7).all()
+        after = [(h.export_state(), h.stats()) for h in w.handles + [small]]
+        for (sa, ca), (sb, cb) in zip(before, after):
+            for x, y in zip(sa, sb):
+                np.testing.assert_array_equal(x, y)
+            assert ca == cb
+        for s in range(3, wl.steps):
+            w.launch_step(s, stream, one_launch=True)
+            for layer, h in enumerate(w.handles):
+                hs.hs_stats(h.h, misses[layer, s])
+        torch.cuda.synchronize()
+        res = GpuResult()
+        res.misses = misses
+        res.out = w.out.cpu().numpy()
+        res.trace = w.topk.cpu().numpy()
+        res.stats = [h.stats() for h in w.handles]
+        res.state = [h.export_state() for h in w.handles]
+        res.workload = w
+        res.policy = 0
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+    finally:
+        small.close()
+        other_b.close()
+        w.close()
+
+
 def test_reset_requests_admits_new_requests():
     """Continuous batching: after 12 steps, batch slots 1 and 4 take new
     requests (slot 4 with a shorter length) and the run goes on.  Those
