@@ -12,14 +12,24 @@
 //
 // The array is a file-scope __device__ variable: every GPU on which the
 // library's module is loaded holds it until the process exits.  From host
-// code its name is only a stand-in, so the device address is looked up once
-// per device with cudaGetSymbolAddress (on the first call made with that
-// device current) and passed to the kernels.  All calls share the array and
-// it keeps the last call's contents; nothing in it has to start at zero (the
+// code its name is only a stand-in, so the device address is looked up per
+// device with cudaGetSymbolAddress (on the first call made with that device
+// current) and passed to the kernels.  That set-up is kept only once it has
+// succeeded: a call that finds it failed tries it again.  It is refused while
+// the call's stream is being captured into a CUDA graph, so the first call on
+// a device must come before any capture.  All calls share the array and it
+// keeps the last call's contents; nothing in it has to start at zero (the
 // resolve kernel writes every list entry and count the copy kernel reads).
 // Calls on one device whose work overlaps on the GPU (for example on two
 // streams) race on that device's array; order them on one stream.  Each
 // device has its own copy of the array.
+//
+// The step itself is the one hs_resolve takes with its defaults -- LRU
+// eviction, the fixed resident tail [C - T, C) -- in two launches: the
+// resolve kernel, then the grid-wide row-copy kernel.
+#include <cuda.h>
+
+#include <atomic>
 #include <cstddef>
 #include <mutex>
 
@@ -35,12 +45,28 @@ constexpr size_t kScratchBytes = 2 * kListEntries * sizeof(int32_t)  // miss tok
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 struct DeviceScratch {
-    std::once_flag once;
-    cudaError_t status = cudaErrorNotReady;
+    std::mutex mu;
+    std::atomic<bool> ready{false};
     unsigned char* ptr = nullptr;
 };
 
 DeviceScratch g_dev[kMaxDevices];
+
+// cuPointerGetAttribute and cuMemGetAddressRange, found through the runtime
+// so that the library does not link the driver library itself.
+using PointerGetAttributeFn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+using GetAddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+std::atomic<PointerGetAttributeFn> g_get_attr{nullptr};
+std::atomic<GetAddressRangeFn> g_get_range{nullptr};
+
+cudaError_t driver_fn(const char* name, void** fn)
+{
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    *fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, CUDA_VERSION, cudaEnableDefault, &q);
+    if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || !*fn)) e = cudaErrorSymbolNotFound;
+    return e;
+}
 
 static_assert(sizeof(hs_control_t) == sizeof(HsDevState), "control block layout");
 static_assert(offsetof(hs_control_t, step) == offsetof(HsDevState, step), "control step");
@@ -49,21 +75,70 @@ static_assert(offsetof(hs_control_t, hits) == offsetof(HsDevState, hits), "contr
 static_assert(offsetof(hs_control_t, misses) == offsetof(HsDevState, misses), "control misses");
 static_assert(offsetof(hs_control_t, inplace) == offsetof(HsDevState, inplace), "control inplace");
 
-// Per-device set-up, run once with that device current: the scratch address
-// and the resolve kernel's shared-memory limit.  Neither allocates.
-DeviceScratch* scratch_for(int dev)
+// Per-device set-up with that device current: the scratch address, the
+// resolve kernel's shared-memory limit and the pointer-attribute query.  None
+// of it allocates.  Returns HS_OK and the scratch address; HS_ERR_ARG when
+// the set-up is still to do and `s` is being captured; HS_ERR_CUDA when a
+// call failed (nothing is kept, so the next call tries again).
+int scratch_for(int dev, cudaStream_t s, unsigned char** out)
 {
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) return HS_ERR_CUDA;
     DeviceScratch* d = &g_dev[dev];
-    std::call_once(d->once, [d]() {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e == cudaSuccess) e = hs_prepare_resolve();
-        d->ptr = static_cast<unsigned char*>(p);
-        d->status = e;
-    });
-    return d->status == cudaSuccess ? d : nullptr;
+    if (!d->ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(d->mu);
+        if (!d->ready.load(std::memory_order_relaxed)) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+                cudaGetLastError();
+                return HS_ERR_CUDA;
+            }
+            if (cs != cudaStreamCaptureStatusNone) return HS_ERR_ARG;
+            void* p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e == cudaSuccess) e = hs_prepare_resolve();
+            void* fa = nullptr;
+            void* fr = nullptr;
+            if (e == cudaSuccess) e = driver_fn("cuPointerGetAttribute", &fa);
+            if (e == cudaSuccess) e = driver_fn("cuMemGetAddressRange", &fr);
+            if (e == cudaSuccess) {
+                g_get_attr.store(reinterpret_cast<PointerGetAttributeFn>(fa));
+                g_get_range.store(reinterpret_cast<GetAddressRangeFn>(fr));
+            }
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return HS_ERR_CUDA;
+            }
+            d->ptr = static_cast<unsigned char*>(p);
+            d->ready.store(true, std::memory_order_release);
+        }
+    }
+    *out = d->ptr;
+    return HS_OK;
 }
+
+// The copy kernel reads B * host_rows * R bytes from the pool: they must lie
+// inside the one pinned allocation that holds its first byte.  The driver
+// reports that allocation's extent (as an address range of the pointer, else
+// as the range of the allocation); memory whose extent it does not know is
+// refused.
+bool pool_inside_allocation(const void* pool_dev, size_t bytes)
+{
+    const CUdeviceptr p = (CUdeviceptr)(uintptr_t)pool_dev;
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    bool known = false;
+    if (PointerGetAttributeFn get = g_get_attr.load())
+        known = get(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, p) == CUDA_SUCCESS &&
+                get(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, p) == CUDA_SUCCESS && size > 0;
+    if (!known) {
+        GetAddressRangeFn range = g_get_range.load();
+        known = range && range(&start, &size, p) == CUDA_SUCCESS && size > 0;
+    }
+    if (!known || p < start || p - start >= size) return false;
+    return bytes <= size - (size_t)(p - start);
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 }  // namespace
 
@@ -88,10 +163,19 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
         row_bytes > HS_MAX_ROW_BYTES || (long long)batch * K > HS_NOALLOC_MAX_ENTRIES)
         return HS_ERR_LIMIT;
 
+    // Alignment the kernels' accesses need: 16-byte row loads and stores,
+    // 64-bit counter atomics in the control block, 32-bit table entries.
+    if (!aligned(host_pool, 16) || !aligned(device_buffer, 16) || !aligned(control, 8) ||
+        !aligned(topk_idx, 4) || !aligned(out_slot, 4) || !aligned(tok_slot, 4) ||
+        !aligned(slot_tok, 4) || !aligned(stamp, 4) || !aligned(lengths, 4))
+        return HS_ERR_ARG;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-    DeviceScratch* d = scratch_for(dev);
-    if (!d) return HS_ERR_CUDA;
+    unsigned char* scratch = nullptr;
+    const int rc = scratch_for(dev, s, &scratch);
+    if (rc != HS_OK) return rc;
 
     // The pool must be pinned and mapped; this looks up its device address.
     void* pool_dev = nullptr;
@@ -99,12 +183,13 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
         cudaGetLastError();
         return HS_ERR_ARG;
     }
+    if (!pool_inside_allocation(pool_dev, (size_t)batch * (size_t)host_rows * (size_t)row_bytes))
+        return HS_ERR_ARG;
 
-    int32_t* miss_tok = reinterpret_cast<int32_t*>(d->ptr);
+    int32_t* miss_tok = reinterpret_cast<int32_t*>(scratch);
     int32_t* miss_slot = miss_tok + (size_t)batch * K;
     int32_t* miss_cnt = miss_tok + 2 * kListEntries;
     HsDevState* st = reinterpret_cast<HsDevState*>(control);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     ResolveArgs ra;
     ra.topk = topk_idx;

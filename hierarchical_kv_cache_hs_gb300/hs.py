@@ -309,6 +309,26 @@ def hs_h2d_read(src_host, dst_dev, nbytes: int, blocks: int = 0, stream=None) ->
 HS_NOALLOC_MAX_ENTRIES = 524288
 
 
+def _check_buffer(x, name, dtype, numel, device=None, pinned=False):
+    """Shape, type and placement of one torch tensor argument of
+    hs_resolve_noalloc (the library cannot see the sizes of caller buffers).
+    Raw addresses are passed through: their sizes are the caller's to keep."""
+    if x is None:
+        raise ValueError("%s is required" % name)
+    if not hasattr(x, "data_ptr") or not hasattr(x, "is_contiguous"):
+        return
+    if x.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, x.dtype))
+    if not x.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if x.numel() < numel:
+        raise ValueError("%s holds %d elements, needs %d" % (name, x.numel(), numel))
+    if device is not None and x.device != device:
+        raise ValueError("%s must be on %s, is on %s" % (name, device, x.device))
+    if pinned and not (x.device.type == "cpu" and x.is_pinned()):
+        raise ValueError("%s must be pinned host memory" % name)
+
+
 def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resident_tail,
                        topk_idx, K, out_slot, tok_slot, slot_tok, stamp, lengths, host_pool,
                        device_buffer, control, stream=None) -> None:
@@ -317,9 +337,25 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
     For callers that cannot let a library allocate device memory (an engine
     that reserved HBM for its own pool, a loop where an allocation would stall
     the device).  ``control`` is a zeroed 32-byte device block (hs_control_t).
+    Torch tensors are checked here (dtype, contiguity, size, device, pinned
+    pool) and a mismatch raises ValueError before the call.
     """
-    _check(lib.hs_resolve_noalloc(int(batch), int(ctx_len), int(row_bytes), int(buffer_slots),
-                                  int(host_rows), int(resident_tail), _ptr(topk_idx), int(K),
+    import torch
+    B, C, R, S, T, K = (int(batch), int(ctx_len), int(row_bytes), int(buffer_slots),
+                        int(resident_tail), int(K))
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else None
+    i32, u8 = torch.int32, torch.uint8
+    _check_buffer(topk_idx, "topk_idx", i32, B * K, dev)
+    _check_buffer(out_slot, "out_slot", i32, B * K, dev)
+    _check_buffer(tok_slot, "tok_slot", i32, B * C, dev)
+    _check_buffer(slot_tok, "slot_tok", i32, B * S, dev)
+    _check_buffer(stamp, "stamp", i32, B * S, dev)
+    _check_buffer(lengths, "lengths", i32, B, dev)
+    _check_buffer(device_buffer, "device_buffer", u8, B * (S + T) * R, dev)
+    if hasattr(control, "element_size"):
+        _check_buffer(control, "control", control.dtype, -(-32 // control.element_size()), dev)
+    _check_buffer(host_pool, "host_pool", u8, B * int(host_rows) * R, pinned=True)
+    _check(lib.hs_resolve_noalloc(B, C, R, S, int(host_rows), T, _ptr(topk_idx), K,
                                   _ptr(out_slot), _ptr(tok_slot), _ptr(slot_tok), _ptr(stamp),
                                   _ptr(lengths), _ptr(host_pool), _ptr(device_buffer),
                                   _ptr(control), _stream(stream)), "hs_resolve_noalloc")
