@@ -121,11 +121,16 @@ typedef struct {
  * (use hs_set_lengths for a growing context).  The host pool is allocated
  * but not filled: write the cold rows through hs_host_pool before resolving.
  * Returns HS_OK and *out, or an HS_ERR_* code (then *out = NULL).
+ * Source: HiSparse blog, "ベンチマークテスト" (the deployment's top_k,
+ * device_buffer_size and host_to_device_ratio); vLLM Hybrid HiSparse post,
+ * "Mixed Residency" (the device-resident tail) and "メモリ管理と統合" (a hot
+ * buffer of 2x top-K rows per request by default).
  */
 int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_ratio,
               int resident_tail, hs_handle** out);
 
-/* Free everything the handle owns.  Synchronises the device first.  NULL is a no-op. */
+/* Free everything the handle owns.  Synchronises the device first.  NULL is a no-op.
+ * Source: no passage (the handle's lifetime; the pages define no API). */
 void hs_destroy(hs_handle* h);
 
 /*
@@ -135,6 +140,11 @@ void hs_destroy(hs_handle* h);
  * Asynchronous; graph-capturable.  Calls on one handle must be ordered (one
  * stream, or streams joined by events): each step reads the state the
  * previous step wrote.
+ * Source: HiSparse blog, "効率的なSwap-inカーネル", steps (1)-(3); papercache
+ * summary, section 2 "方法细节"; vLLM Hybrid HiSparse post, "Mixed Residency"
+ * (tail tokens in place, a hit refreshes its LRU entry, a miss copies one row
+ * from pinned host memory into the LRU slot, no wait on the CPU) and "No
+ * Residency" (a request starts with an empty buffer).
  */
 int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                hs_stream_t stream);
@@ -148,6 +158,8 @@ int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
  * gets the slot of its first occurrence and is fetched and counted once.
  * out_slot is [B][P][K].  1 <= P*K <= min(S, HS_MAX_TOPK).  A retried step
  * is simply another call.  Asynchronous; graph-capturable.
+ * Source: vLLM Hybrid HiSparse post, "vLLM エコシステムとの統合", item
+ * "Speculative Decoding".
  */
 int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_t* out_slot,
                      hs_stream_t stream);
@@ -167,6 +179,9 @@ int hs_resolve_multi(hs_handle* h, const int32_t* topk_idx, int P, int K, int32_
  * 1 <= K <= min(S, HS_MAX_TOPK).  Asynchronous; graph-capturable.  Errors:
  * HS_ERR_ARG (a NULL array, entry or handle, a handle given twice, shapes
  * that differ, another device), HS_ERR_TOPK_GT_SLOTS, HS_ERR_LIMIT.
+ * Source: HiSparse blog, "今後の展望", and papercache summary, section 4
+ * "结论与未来工作" (better overlap as the way to cut the miss I/O overhead);
+ * the per-layer step is hs_resolve's.
  */
 int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
                       int32_t* const* out_slot, hs_stream_t stream);
@@ -176,6 +191,10 @@ int hs_resolve_layers(hs_handle* const* handles, int L, const int32_t* const* to
  * buffers ([B][K] each), with the same rules as hs_resolve_host (mapped
  * pinned buffers are read and written by the kernel directly, others are
  * staged); synchronises the stream before returning.  Not graph-capturable.
+ * Every check of hs_resolve_layers is made before anything is staged or
+ * enqueued.
+ * Source: as hs_resolve_layers; the host buffers are this library's end-to-end
+ * entry, with no passage of their own.
  */
 int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* const* topk_idx, int K,
                            int32_t* const* out_slot, hs_stream_t stream);
@@ -191,6 +210,8 @@ int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* cons
  * memory (a Grace host), it can accept ordinary malloc'd buffers too, and
  * those are then read and written in place as well.  Not graph-capturable
  * (it synchronises).
+ * Source: as hs_resolve; the host buffers are this library's end-to-end
+ * entry, with no passage of their own.
  */
 int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                     hs_stream_t stream);
@@ -205,6 +226,9 @@ int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_s
  * hs_resolve.  Not graph-capturable.  The first call allocates the staging
  * areas (B * min(S, HS_MAX_TOPK) rows on the host and on the device) and
  * starts the host threads.
+ * Source: HiSparse blog, "効率的なSwap-inカーネル", step (3) (fetch the
+ * needed entries from host into device memory), done here by the copy engine
+ * instead of the kernel, for comparison.
  */
 int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                   hs_stream_t stream);
@@ -212,20 +236,29 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
 /*
  * Read the counters and, if last_miss is not NULL, the last step's miss count
  * of every request (host, [B]).  Synchronises the device first.
+ * Source: HiSparse blog, "効率的なSwap-inカーネル" (the figure of miss counts
+ * against hot-buffer size and eviction strategy: misses are the path's own
+ * measure).
  */
 int hs_stats(hs_handle* h, hs_stats_t* out, int32_t* last_miss);
 
-/* Host pointer of the pinned, device-mapped host pool [B][H][R]; its size in bytes. */
+/* Host pointer of the pinned, device-mapped host pool [B][H][R]; its size in bytes.
+ * Source: HiSparse blog, "HiSparseの設計" (inactive KV entries are offloaded to
+ * host memory); vLLM Hybrid HiSparse post, "Mixed Residency" (pinned host memory). */
 uint8_t* hs_host_pool(hs_handle* h);
 size_t hs_host_pool_bytes(hs_handle* h);
 
-/* Device pointer of the buffer [B][S+T][R] that out_slot indexes; its size in bytes. */
+/* Device pointer of the buffer [B][S+T][R] that out_slot indexes; its size in bytes.
+ * Source: HiSparse blog, "HiSparseの設計" (the hot device buffer in HBM);
+ * vLLM Hybrid HiSparse post, "Mixed Residency" (the tail stays on the GPU). */
 uint8_t* hs_device_buffer(hs_handle* h);
 size_t hs_device_buffer_bytes(hs_handle* h);
 
 /*
  * Set the current length of every request (host, [B]; each in [0, C]).
  * Setup only: synchronises the device first.
+ * Source: vLLM Hybrid HiSparse post, "エージェント的ワークロードにおける KV
+ * キャッシュ圧迫の解決" (contexts that grow over time) and "Mixed Residency".
  */
 int hs_set_lengths(hs_handle* h, const int32_t* len_host);
 
@@ -237,6 +270,9 @@ int hs_set_lengths(hs_handle* h, const int32_t* len_host);
  * sliding tail (hs_set_tail_mode) only len[b] = C is refused, and the token
  * leaving the tail is first written back to the host pool.  Asynchronous;
  * graph-capturable.  Requires T > 0.
+ * Source: vLLM Hybrid HiSparse post, "Mixed Residency" (the request's tail
+ * stays on the GPU) and "Full Residency" (pages copied to host memory ahead
+ * of eviction, the sliding tail's write-back).
  */
 int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream);
 
@@ -244,6 +280,8 @@ int hs_append(hs_handle* h, const uint8_t* rows_dev, hs_stream_t stream);
  * Setup only: write tokens [first_token, first_token + n) of request b from
  * rows_host (host, [n][R]) into their tail slots S + (t mod T).  All tokens
  * must lie in [C - T, C).  Synchronous.
+ * Source: vLLM Hybrid HiSparse post, "Mixed Residency" (the tail rows live
+ * on the device).
  */
 int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t* rows_host);
 
@@ -251,6 +289,7 @@ int hs_set_tail_rows(hs_handle* h, int b, int first_token, int n, const uint8_t*
  * Copy the state to host memory (any pointer may be NULL to skip it):
  * tok_slot [B][C], slot_tok [B][S], stamp [B][S], step (one int32).
  * Synchronises the device first.
+ * Source: no passage (a test, checkpoint and resume aid).
  */
 int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp,
                     int32_t* step);
@@ -264,15 +303,19 @@ int hs_export_state(hs_handle* h, int32_t* tok_slot, int32_t* slot_tok, int32_t*
  * two maps inverse to each other, every stamp in [0, step], 0 <= step <= HS_MAX_STEP.
  * Buffer bytes are not part of the state (write them, or let misses refill
  * them).  Counters and error bits are cleared.  Synchronous.
+ * Source: no passage (a test, checkpoint and resume aid).
  */
 int hs_import_state(hs_handle* h, const int32_t* tok_slot, const int32_t* slot_tok,
                     const int32_t* stamp, int32_t step);
 
-/* Copy request b's buffer rows [S+T][R] to host memory.  Synchronous. */
+/* Copy request b's buffer rows [S+T][R] to host memory.  Synchronous.
+ * Source: no passage (a test, checkpoint and resume aid). */
 int hs_export_buffer(hs_handle* h, int b, uint8_t* dst_host);
 
 /* Back to the start state: empty tables, stamps 0, step 0, counters and error bits 0,
- * lengths = C.  The host pool and buffer bytes are kept.  Synchronous. */
+ * lengths = C.  The host pool and buffer bytes are kept.  Synchronous.
+ * Source: vLLM Hybrid HiSparse post, "No Residency" (the start state: placeholders
+ * only, rows loaded when the indexer selects them). */
 int hs_reset(hs_handle* h);
 
 /*
@@ -288,6 +331,7 @@ int hs_reset(hs_handle* h);
  * [0, B) or a length outside [0, C] is skipped and latches HS_E_RANGE; a
  * repeated id is reset once more.  0 <= n <= HS_MAX_BATCH.  Asynchronous and
  * graph-capturable, ordered with the handle's other calls by the stream.
+ * Source: vLLM Hybrid HiSparse post, "No Residency".
  */
 int hs_reset_requests(hs_handle* h, const int32_t* req_ids, int n, const int32_t* lengths,
                       hs_stream_t stream);
@@ -298,6 +342,8 @@ int hs_reset_requests(hs_handle* h, const int32_t* req_ids, int n, const int32_t
  * or returned by hs_host_pool) into device memory `dst_dev` with 128-bit
  * zero-copy loads -- the access pattern of the row fetch, but sequential.
  * `blocks` = 0 picks the default grid.  Asynchronous.
+ * Source: HiSparse blog, "今後の展望" (the CPU-GPU bandwidth of Grace
+ * Blackwell systems bounds the miss I/O); this probe measures it.
  */
 int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
                 hs_stream_t stream);
@@ -313,6 +359,8 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
  *                  HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
  *                  much to copy; split otherwise (default).  A function of the
  *                  handle alone, so hs_resolve_launches answers per handle.
+ * Source: HiSparse blog, "効率的なSwap-inカーネル" (one dedicated kernel does
+ * steps (1)-(3)); the split form is this library's, with no passage.
  */
 #define HS_COPY_AUTO   0
 #define HS_COPY_FUSED  1
@@ -331,6 +379,8 @@ int hs_set_copy_mode(hs_handle* h, int mode);
  *                   step that hits it).
  * Ties go to the lowest slot index under both.  Takes effect at the next
  * hs_resolve; switching mid-run keeps the stamps as they are.
+ * Source: HiSparse blog, "効率的なSwap-inカーネル"; papercache summary,
+ * section 2 "方法细节" (the eviction strategy is one axis of the miss count).
  */
 #define HS_POLICY_LRU   0
 #define HS_POLICY_FIFO  1
@@ -348,12 +398,14 @@ int hs_set_policy(hs_handle* h, int policy);
  *                    "Full Residency" pre-copy).  hs_set_tail_rows then takes
  *                    any token below C: write the current last T tokens.
  * Setup only (before the first hs_resolve); sliding needs resident_tail > 0.
+ * Source: vLLM Hybrid HiSparse post, "Mixed Residency" and "Full Residency".
  */
 #define HS_TAIL_FIXED    0
 #define HS_TAIL_SLIDING  1
 int hs_set_tail_mode(hs_handle* h, int mode);
 
-/* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG. */
+/* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG.
+ * Source: no passage (a measurement aid). */
 int hs_resolve_launches(hs_handle* h);
 
 /*
@@ -363,34 +415,48 @@ int hs_resolve_launches(hs_handle* h);
  * (fused mode), so that kernel's duration can be read with
  * cudaEventElapsedTime.  In split mode the copy then no longer overlaps the
  * tail of the resolve kernel.  Pass NULL, NULL to switch it off.
+ * Source: no passage (a measurement aid).
  */
 int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy);
 
 /*
  * ---- Allocation-free variant -------------------------------------------
- * (The pages have no counterpart: this entry point exists for callers of the
- * library, not because the method needs it.)
+ * Source: no passage -- the pages have no counterpart: this entry point exists
+ * for callers of the library, not because the method needs it.
  *
  * For callers that must not have a library allocate device memory -- an
  * engine that has reserved nearly all HBM for its own KV pool, or a decode
  * loop in which an allocation would synchronise the device.  The caller owns
- * all state and passes it in; the step is the same as hs_resolve's.
+ * all state and passes it in.  The step is hs_resolve's with a handle's
+ * defaults, and only those: LRU eviction, the fixed resident tail [C - T, C),
+ * one top-k row per request, and two launches (the resolve kernel, then the
+ * grid-wide row-copy kernel; HS_COPY_SPLIT).
  *
  *   tok_slot [B][C], slot_tok [B][S] (start at -1), stamp [B][S] (start at 0),
  *   lengths [B], device_buffer [B][S+T][R]: device memory.
  *   host_pool [B][host_rows][R]: pinned host memory mapped into the device
- *   address space (cudaHostAlloc with cudaHostAllocMapped), host pointer.
+ *   address space (cudaHostAlloc with cudaHostAllocMapped), host pointer;
+ *   all B * host_rows * R bytes must lie in the allocation that holds its
+ *   first byte, as the driver reports it.
  *   control: device memory, one hs_control_t, zeroed by the caller before
  *   the first step; the step counter and counters advance in it.
+ * Alignment: host_pool and device_buffer 16 bytes, control 8 bytes, the
+ * int32 arrays 4 bytes.  A pointer that breaks it, a pool whose extent the
+ * driver does not know or that is shorter than B * host_rows * R bytes, is
+ * refused with HS_ERR_ARG before anything is enqueued.  The tables are not
+ * checked on the host; the kernels check every entry they would use as an
+ * index and repair and flag what is out of range (HS_E_STATE).
  *
  * The per-step miss lists live in a fixed device array inside the library
  * (HS_NOALLOC_SCRATCH_BYTES, held on every device that loads the library
  * until the process exits), so B * K may not exceed HS_NOALLOC_MAX_ENTRIES
  * (HS_ERR_LIMIT otherwise).  The first call on a device looks up that
  * array's address and sets kernel attributes; make that first call before
- * any stream capture.  All calls on a device share the array: calls whose
- * work overlaps on the GPU race, so order them on one stream.  Returns
- * HS_OK or an HS_ERR_* code, synchronously, like hs_resolve.
+ * any stream capture (while `stream` is being captured, a call that would do
+ * it returns HS_ERR_ARG and enqueues nothing).  A set-up that failed is not
+ * kept: the next call tries it again.  All calls on a device share the
+ * array: calls whose work overlaps on the GPU race, so order them on one
+ * stream.  Returns HS_OK or an HS_ERR_* code, synchronously, like hs_resolve.
  */
 #define HS_NOALLOC_MAX_ENTRIES    524288   /* B * K */
 #define HS_NOALLOC_SCRATCH_BYTES  (2 * 4 * HS_NOALLOC_MAX_ENTRIES + 4 * HS_MAX_BATCH)
@@ -409,7 +475,7 @@ int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buffer_slots, 
                        const int32_t* lengths, const uint8_t* host_pool, uint8_t* device_buffer,
                        hs_control_t* control, hs_stream_t stream);
 
-/* Static text for a return code. */
+/* Static text for a return code.  Source: no passage. */
 const char* hs_error_string(int code);
 
 #ifdef __cplusplus
