@@ -36,18 +36,82 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 PRIME_STEPS = 10
-# DRAM (read + write) and host-link read bytes of one steady-state launch of the
-# fused swap-in kernel on the 64-request, 64K-context, 4096-slot workload, from
-# its ncu capture (profiles/hs_resolve_kernel_fused_b64_c64k_s4096.md).  The
-# host-link bytes equal the algorithmic miss-row bytes of that launch.
-FUSED_NCU_DRAM_BYTES = 9070848 + 779008
-FUSED_NCU_SYSMEM_BYTES = 933264 * 32
-# The same for the one-launch layers kernel on the 4-layer, 64-request,
-# 128K-context workload (profiles/hs_resolve_layers_kernel_b64_c128k_l4.md).
-LAYERS_NCU_DRAM_BYTES = 45681408 + 66817024
-LAYERS_NCU_SYSMEM_BYTES = 3410100 * 32
+# DRAM and host-link bytes of one steady-state launch per (kernel, workload),
+# written from ncu captures together with the fingerprint of the kernel's code
+# at the time of the capture.  A figure whose fingerprint no longer matches is
+# not reported (the kernel has changed since it was measured).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+# The files that define each kernel's code.
+KERNEL_SOURCES = {
+    "hs_resolve_kernel_fused": ["hs_resolve.cu", "hs_internal.h"],
+    "hs_resolve_layers_kernel": ["hs_resolve.cu", "hs_internal.h"],
+    "hs_copy_kernel": ["hs_copy.cu", "hs_internal.h"],
+}
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20
+# Config keys shared word for word by both arms, so that their lines describe
+# the same run.
+CONFIG_L2 = ("GPU arm: L2 flushed before every timed step (256 MiB write, outside the timed "
+             "events); the oracle arm runs on the host cores")
+CONFIG_PARALLELISM = "requests sharded over ranks, no collective on the data path"
+# The pages' own figures: end-to-end serving results on other hardware, quoted
+# as context only (no number of the pages measures the swap-in path itself).
+CONTEXT = {
+    "note": "the pages' end-to-end serving results on other hardware; context only, not a "
+            "kernel result and not the target",
+    "figures": [
+        {"result": "more than 3x the decode throughput of sparse attention without HiSparse",
+         "at": "256 concurrent requests, 32K input / 8K output",
+         "hardware": "one node of 8xH200, prefill and decode colocated",
+         "settings": "top_k 2048, device_buffer_size 4096, host_to_device_ratio 8",
+         "source": "papercache summary, section 1 and section 3; HiSparse blog, introduction "
+                   "and 'ベンチマークテスト'"},
+        {"result": "up to 5x throughput in long-context settings",
+         "at": "a sweep of input / output lengths",
+         "hardware": "two nodes of H20, prefill and decode disaggregated",
+         "settings": "top_k 2048, device_buffer_size 6144, host_to_device_ratio 10",
+         "source": "HiSparse blog, 'ベンチマークテスト'; papercache summary, section 3"},
+    ],
+}
+
+
+def _config(wl):
+    return {"workload": _workload_desc(wl), "prime_steps_untimed": PRIME_STEPS, "l2": CONFIG_L2,
+            "parallelism": CONFIG_PARALLELISM}
+
+
+def _code_fingerprint(names):
+    """First 16 hex digits of the SHA-256 of the given csrc files' code, with
+    comments and whitespace removed (a comment edit leaves it unchanged)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "hierarchical_kv_cache_hs_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + b"\0" + " ".join(text.split()).encode() + b"\0")
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel, workload):
+    """(DRAM read + write bytes, host-link read bytes, note) of one launch of
+    `kernel` on `workload` from the traffic file, or (None, None, why not)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    except OSError:
+        return None, None, "no ncu capture on file"
+    now = _code_fingerprint(KERNEL_SOURCES[kernel])
+    for r in rows:
+        if len(r) >= 7 and r[0] == kernel and r[1] == workload:
+            if r[5] != now:
+                return None, None, ("stale: captured on kernel code %s, the code is now %s"
+                                    % (r[5], now))
+            return int(r[2]) + int(r[3]), int(r[4]), ("ncu capture of one steady-state launch at "
+                                                      "commit %s, kernel code %s" % (r[6], now))
+    return None, None, "no ncu capture of this kernel on this workload"
 
 
 def _workload_desc(wl):
@@ -243,7 +307,9 @@ def run_ours(args, rank, world, dist):
         peaks = measure_h2d_peak(torch, hs)
     hbm_gbs, hbm_src = measure_hbm_peak(torch)
 
-    def measure(wl, want_profile=True, want_e2e=True, want_ce=False):
+    def measure(wl, want_profile=True, want_e2e=True, want_ce=False, one_launch=None):
+        # Several layers: one launch for all of them, or one call per layer.
+        one = (args.layer_launch == "one" and wl.layers > 1) if one_launch is None else one_launch
         w = GpuWorkload(wl, steps=total_steps, record=False, host_trace=want_e2e,
                         request_offset=shard_requests(rank, wl.B)[0], copy_mode=mode)
         stream = torch.cuda.Stream(device=dev)
@@ -263,6 +329,7 @@ def run_ours(args, rank, world, dist):
                     w.launch_step(s, stream, one_launch=one)
                 stream.synchronize()
                 m0 = stats_sum("misses")
+                i0 = stats_sum("inplace")
                 barrier()
                 torch.cuda.synchronize()
                 t_wall0 = time.perf_counter()
@@ -279,7 +346,7 @@ def run_ours(args, rank, world, dist):
             dev_ms = sum(step_ms)
             miss_rows = stats_sum("misses") - m0
             res.update(dev_ms=dev_ms, step_ms=step_ms, wall_s=t_wall, launches=launches,
-                       miss_rows=miss_rows)
+                       miss_rows=miss_rows, inplace=stats_sum("inplace") - i0)
 
             # --- per-step miss counts + copy-kernel durations (second pass) ----
             if want_profile:
@@ -370,8 +437,7 @@ def run_ours(args, rank, world, dist):
         return res
 
     sampler = ClockSampler(dev.index, args.clocks_csv)
-    main = measure(wl, want_e2e=not args.no_e2e, want_ce=not args.no_ce)
-    fused = main["fused"]
+    main = measure(wl, want_e2e=not args.no_e2e, want_ce=not args.no_ce, one_launch=one)
     clocks = sampler.stop()
 
     def policy_sweep(wl):
@@ -416,10 +482,12 @@ def run_ours(args, rank, world, dist):
                             hs.hs_stats(h.h, last)
                             tot += int(last.sum())
                         per_step.append(tot)
+                gbs = sum(per_step) * wl.row_bytes / (ms / 1e3) / 1e9
                 out[pname] = {
                     "resolves_per_s": wl.B * wl.layers * args.steps / (ms / 1e3),
                     "ms_per_step": ms / args.steps,
-                    "miss_row_gbs": sum(per_step) * wl.row_bytes / (ms / 1e3) / 1e9,
+                    "miss_row_gbs": gbs,
+                    "miss_row_frac_of_h2d_peak": gbs / peaks["peak_gbs"],
                     "misses_per_step_mean": statistics.mean(per_step),
                     "misses_per_step": per_step,
                 }
@@ -432,87 +500,90 @@ def run_ours(args, rank, world, dist):
         for name in ("b64_c64k_s4096", "b64_c64k_s2048"):
             sweep[name] = policy_sweep(tg.WORKLOADS[name])
 
-    units = wl.B * wl.layers * args.steps
-    dev_s = max_over_ranks(main["dev_ms"] / 1e3)
-    all_units = sum_over_ranks(units)
-    value = all_units / dev_s
-    miss_bytes = main["miss_rows"] * wl.row_bytes
-    miss_gbs = sum_over_ranks(miss_bytes) / dev_s / 1e9
-    h2d_peak = peaks["peak_gbs"]
+    def summarize(wl, res, one):
+        """The metric, both rooflines and the end-to-end figure of one measured workload."""
+        fused = res["fused"]
+        units = wl.B * wl.layers * args.steps
+        dev_s = max_over_ranks(res["dev_ms"] / 1e3)
+        all_units = sum_over_ranks(units)
+        value = all_units / dev_s
+        miss_gbs = sum_over_ranks(res["miss_rows"] * wl.row_bytes) / dev_s / 1e9
+        h2d_peak = peaks["peak_gbs"]
+        # Roofline of the dominant kernel (the swap-in kernel, or the row copy in
+        # split mode): algorithmic bytes are the miss rows (R bytes each) read over
+        # the host link, per launch.
+        copy_s = sum(res["copy_ms"]) / 1e3
+        copy_gbs = (sum(res["misses_per_step"]) * wl.row_bytes) / copy_s / 1e9
+        # Whole-step roofline: max(miss bytes / H2D peak, table bytes / HBM peak).
+        t_roof = 0.0
+        for m in res["misses_per_step"]:
+            table = wl.layers * (wl.B * (16 * wl.K + 4 * wl.S)) + 16 * m
+            t_roof += max(m * wl.row_bytes / (h2d_peak * 1e9), table / (hbm_gbs * 1e9))
+        kernel = ("hs_resolve_layers_kernel" if one else "hs_resolve_kernel_fused" if fused
+                  else "hs_copy_kernel")
+        traffic, host_link, traffic_src = dram_traffic(kernel, wl.name)
+        e2e_value = all_units / max_over_ranks(res["e2e_s"]) if "e2e_s" in res else None
+        out = {
+            "value": value,
+            "ms_per_step": res["dev_ms"] / args.steps,
+            "miss_row_gbs": miss_gbs,
+            "miss_row_frac_of_h2d_peak": miss_gbs / h2d_peak,
+            "step_roofline": {"t_roof_ms_per_step": t_roof * 1e3 / args.steps,
+                              "frac": t_roof / (res["dev_ms"] / 1e3),
+                              "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
+                              "table_bytes_per_resolve": "16K + 4S + 16m"},
+            "roofline": {"bound": "h2d",
+                         "kernel": ("hs_resolve_layers_kernel (every layer's resolve + row fetch, "
+                                    "one grid)" if one else
+                                    "hs_resolve_kernel<fused> (resolve + row fetch)" if fused
+                                    else "hs_copy_kernel"),
+                         "achieved": copy_gbs,
+                         "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
+                         "traffic": traffic,
+                         "traffic_host_link": host_link,
+                         "traffic_source": traffic_src,
+                         "peak_source": "measured in this run: max(1 GiB pinned->device "
+                                        "cudaMemcpyAsync, 1 GiB zero-copy 128-bit read kernel)"},
+            "kernel_ms_per_step": ({"swapin_fused": sum(res["copy_ms"]) / args.steps}
+                                   if (fused or one) else
+                                   {"copy": sum(res["copy_ms"]) / args.steps,
+                                    "resolve": sum(res["resolve_ms"]) / args.steps}),
+            "launch_mode": ("fused, all layers in one launch" if one else "fused" if fused
+                            else "split"),
+            "misses_per_step_mean": statistics.mean(res["misses_per_step"]),
+            "inplace_per_step_mean": res["inplace"] / args.steps,
+            "e2e": {"value": e2e_value, "unit": "resolves/s",
+                    "h2d_bytes_per_step": wl.layers * wl.B * wl.K * 4,
+                    "d2h_bytes_per_step": wl.layers * wl.B * wl.K * 4,
+                    "api": ("hs_resolve_layers_host" if one else "hs_resolve_host") +
+                           " (pinned host top-k in, host out_slot back, synchronised)"},
+        }
+        return out
 
-    # Roofline of the dominant kernel (row copy): algorithmic bytes are the
-    # miss rows (R bytes each) read over the host link, per launch.
-    copy_s = sum(main["copy_ms"]) / 1e3
-    copy_gbs = (sum(main["misses_per_step"]) * wl.row_bytes) / copy_s / 1e9
-    # Whole-step roofline: max(miss bytes / H2D peak, table bytes / HBM peak).
-    t_roof = 0.0
-    for m in main["misses_per_step"]:
-        table = wl.layers * (wl.B * (16 * wl.K + 4 * wl.S)) + 16 * m
-        t_roof += max(m * wl.row_bytes / (h2d_peak * 1e9), table / (hbm_gbs * 1e9))
-    step_frac = t_roof / (main["dev_ms"] / 1e3)
-
-    e2e_value = all_units / max_over_ranks(main["e2e_s"]) if "e2e_s" in main else None
-    launch_mode = "fused, all layers in one launch" if one else "fused" if fused else "split"
+    head = summarize(wl, main, one)
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": head["value"],
         "unit": "resolves/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": main["dev_ms"] / args.steps,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "int32",
         "data": "synthetic (seeded top-k traces and uniform random KV row bytes)",
-        "config": {
-            "workload": _workload_desc(wl),
-            "prime_steps_untimed": PRIME_STEPS,
-            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
-            "parallelism": "requests sharded over ranks, no collective on the data path",
-            "launch_mode": launch_mode,
-        },
-        "miss_row_gbs": miss_gbs,
-        "h2d_peak": peaks,
-        "miss_row_frac_of_h2d_peak": miss_gbs / h2d_peak,
-        "step_roofline": {"t_roof_ms_per_step": t_roof * 1e3 / args.steps,
-                          "frac": step_frac,
-                          "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
-                          "table_bytes_per_resolve": "16K + 4S + 16m"},
-        "roofline": {"bound": "h2d",
-                     "kernel": ("hs_resolve_layers_kernel (every layer's resolve + row fetch, one grid)"
-                                if one else "hs_resolve_kernel<fused> (resolve + row fetch)"
-                                if fused else "hs_copy_kernel"),
-                     "achieved": copy_gbs,
-                     "peak": h2d_peak, "unit": "GB/s", "frac": copy_gbs / h2d_peak,
-                     # ncu, one steady-state launch of this kernel on this workload
-                     # (the summaries under profiles/); None when another kernel or
-                     # workload is timed
-                     "traffic": (FUSED_NCU_DRAM_BYTES if (fused and not one and wl.name == "b64_c64k_s4096")
-                                 else LAYERS_NCU_DRAM_BYTES if (one and wl.name == "b64_c128k_l4_tail4096")
-                                 else None),
-                     "traffic_host_link": (FUSED_NCU_SYSMEM_BYTES if (fused and not one and wl.name == "b64_c64k_s4096")
-                                           else LAYERS_NCU_SYSMEM_BYTES if (one and wl.name == "b64_c128k_l4_tail4096")
-                                           else None),
-                     "peak_source": "measured in this run: max(1 GiB pinned->device cudaMemcpyAsync, "
-                                    "1 GiB zero-copy 128-bit read kernel)"},
-        "kernel_ms_per_step": ({"swapin_fused": sum(main["copy_ms"]) / args.steps} if (fused or one) else
-                               {"copy": sum(main["copy_ms"]) / args.steps,
-                                "resolve": sum(main["resolve_ms"]) / args.steps}),
-        "launch_mode": launch_mode,
-        "misses_per_step_mean": statistics.mean(main["misses_per_step"]),
-        "misses_per_step": main["misses_per_step"],
-        "e2e": {"value": e2e_value, "unit": "resolves/s",
-                "h2d_bytes_per_step": wl.layers * wl.B * wl.K * 4,
-                "d2h_bytes_per_step": wl.layers * wl.B * wl.K * 4,
-                "api": ("hs_resolve_layers_host" if one else "hs_resolve_host") +
-                       " (pinned host top-k in, host out_slot back, synchronised)"},
-        "gpu_launches": main["launches"],
-        "clocks": clocks,
-        "wall_s_timed_region": main["wall_s"],
-        "step_ms_quantiles": _quantiles(main["step_ms"]),
+        "config": _config(wl),
     }
+    line.update({k: v for k, v in head.items() if k not in ("value", "ms_per_step")})
+    line["h2d_peak"] = peaks
+    line["misses_per_step"] = main["misses_per_step"]
+    line["gpu_launches"] = main["launches"]
+    line["clocks"] = clocks
+    line["wall_s_timed_region"] = main["wall_s"]
+    line["step_ms_quantiles"] = _quantiles(main["step_ms"])
+    line["context"] = CONTEXT
     if args.overlap and rank == 0:
         line["layer_overlap"] = layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev)
     if "ce_s" in main:
@@ -523,12 +594,36 @@ def run_ours(args, rank, world, dist):
             "resolves_per_s": ce_value,
             "ms_per_step": main["ce_s"] * 1e3 / main["ce_steps"],
             "steps": main["ce_steps"],
-            "faster": "zero-copy (hs_resolve)" if value > ce_value else "copy-engine (hs_resolve_ce)",
+            "faster": ("zero-copy (hs_resolve)" if head["value"] > ce_value
+                       else "copy-engine (hs_resolve_ce)"),
         }
     if sweep:
         line["sweep"] = sweep
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args, total_steps)
+
+    # Every other workload, each at its own sizes, with the same steps and
+    # warm-up: the parity-test workloads measured by the same passes.
+    if not args.no_configs:
+        per = {}
+        for name in args.configs.split(","):
+            if name == wl.name or not name:
+                continue
+            cw = tg.WORKLOADS[name]
+            c_one = args.layer_launch == "one" and cw.layers > 1
+            sampler = ClockSampler(dev.index)
+            res = measure(cw, want_e2e=not args.no_e2e, one_launch=c_one)
+            c_clocks = sampler.stop()
+            entry = {"workload": _workload_desc(cw), "steps": args.steps, "warmup": args.warmup}
+            entry.update(summarize(cw, res, c_one))
+            entry["gpu_launches"] = res["launches"]
+            entry["clocks"] = c_clocks
+            entry["step_ms_quantiles"] = _quantiles(res["step_ms"])
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline(cw, args, total_steps, host_bytes=CONFIG_ORACLE_HOST_BYTES,
+                                                     single_core=False)
+            per[name] = entry
+        line["configs"] = per
     return line
 
 
@@ -570,13 +665,18 @@ def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
 
 # ---------------------------------------------------------------- CPU oracle
 ORACLE_HOST_BYTES = 8 << 30  # host rows the oracle legs may hold at once
+CONFIG_ORACLE_HOST_BYTES = 1 << 30  # the same for the other workloads' legs
+# The five workloads, in the order of the pages' configurations; the bench
+# workload is the headline line, the others go under "configs".
+CONFIG_WORKLOADS = ("tiny_b1_c8k", "b32_c32k_s4096", "b64_c64k_s4096", "b64_c64k_s2048",
+                    "b256_c32k_grow_tail512", "b64_c128k_l4_tail4096")
 
 
-def _oracle_sample(wl):
+def _oracle_sample(wl, host_bytes=ORACLE_HOST_BYTES):
     """Requests the oracle legs replay: all of them, or the first n whose host
-    rows (every layer) fit in ORACLE_HOST_BYTES."""
+    rows (every layer) fit in host_bytes."""
     per_request = wl.layers * wl.cold * wl.row_bytes
-    n = max(1, min(wl.B, ORACLE_HOST_BYTES // max(per_request, 1)))
+    n = max(1, min(wl.B, host_bytes // max(per_request, 1)))
     return list(range(n))
 
 
@@ -626,23 +726,25 @@ def _sample_desc(wl, requests):
     return who + layers + grow
 
 
-def cpu_baseline(wl, args, total_steps):
+def cpu_baseline(wl, args, total_steps, host_bytes=ORACLE_HOST_BYTES, single_core=True):
     """The oracle as it stands on every host core (and on one), over a bounded
     sample of the workload's requests."""
     cores = _cores()
     from_step = PRIME_STEPS + args.warmup
-    reqs = _oracle_sample(wl)
+    reqs = _oracle_sample(wl, host_bytes)
     secs = _oracle_requests(wl, total_steps, reqs, cores, from_step)
     n = len(reqs) * wl.layers * (total_steps - from_step)
-    # The same on one core, over the first few requests.
-    reqs1 = reqs[:min(8, len(reqs))]
-    secs1 = _oracle_requests(wl, total_steps, reqs1, 1, from_step)
-    return {"value": n / secs, "unit": "resolves/s", "cores": cores, "kind": "oracle",
-            "sample": "the timed steps of the same trace, %s, one request per thread per step, "
-                      "after replaying the untimed prefix" % _sample_desc(wl, reqs),
-            "single_core": {"value": len(reqs1) * wl.layers * (total_steps - from_step) / secs1,
-                            "unit": "resolves/s", "cores": 1,
-                            "sample": "the same timed steps, %s" % _sample_desc(wl, reqs1)}}
+    out = {"value": n / secs, "unit": "resolves/s", "cores": cores, "kind": "oracle",
+           "sample": "the timed steps of the same trace, %s, one request per thread per step, "
+                     "after replaying the untimed prefix" % _sample_desc(wl, reqs)}
+    if single_core:
+        # The same on one core, over the first few requests.
+        reqs1 = reqs[:min(8, len(reqs))]
+        secs1 = _oracle_requests(wl, total_steps, reqs1, 1, from_step)
+        out["single_core"] = {"value": len(reqs1) * wl.layers * (total_steps - from_step) / secs1,
+                              "unit": "resolves/s", "cores": 1,
+                              "sample": "the same timed steps, %s" % _sample_desc(wl, reqs1)}
+    return out
 
 
 def run_reference(args):
@@ -668,7 +770,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "int32",
         "data": "synthetic (seeded top-k traces and uniform random KV row bytes)",
-        "config": {"workload": _workload_desc(wl), "prime_steps_untimed": PRIME_STEPS},
+        "config": _config(wl),
         "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": cores, "kind": "oracle",
                          "sample": "every timed step of the workload, %s, one request per thread"
                                    % _sample_desc(wl, reqs)},
@@ -685,6 +787,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b64_c64k_s4096")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (the \"configs\" key)")
+    ap.add_argument("--configs", default=",".join(CONFIG_WORKLOADS),
+                    help="comma-separated workloads measured under \"configs\" besides --workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the 1 GiB link-peak measurement (profiling runs; no roofline fraction)")

@@ -17,7 +17,8 @@ def test_our_arm_prints_a_complete_line():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "b32_c32k_s4096",
-                        "--steps", "5", "--warmup", "3", "--no-sweep", "--no-ce", "--no-cpu-baseline"],
+                        "--steps", "5", "--warmup", "3", "--no-sweep", "--no-ce", "--no-cpu-baseline",
+                        "--configs", "tiny_b1_c8k"],
                        capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
@@ -38,3 +39,11 @@ def test_our_arm_prints_a_complete_line():
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 32 * 2048 * 4
     assert line["config"]["workload"].startswith("b32_c32k_s4096")
+    # the same config keys as the reference arm, the pages' figures as context
+    assert set(line["config"]) == {"workload", "prime_steps_untimed", "l2", "parallelism"}
+    assert len(line["context"]["figures"]) == 2
+    # the other workload, measured by the same passes
+    tiny = line["configs"]["tiny_b1_c8k"]
+    assert tiny["value"] > 0 and tiny["steps"] == 5 and tiny["roofline"]["frac"] > 0
+    assert tiny["step_roofline"]["frac"] > 0 and tiny["e2e"]["value"] > 0
+    assert abs(tiny["value"] - 1 / (tiny["ms_per_step"] / 1e3)) / tiny["value"] < 1e-6
