@@ -39,7 +39,7 @@ def test_noalloc_matches_handle_path(resident_tail):
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
 
     wl = tg.Workload("noalloc_check", 98, B=8, C=16384 + resident_tail, K=1024, S=1024,
-                     T=resident_tail, host_ratio=8, layers=1, steps=2, len0=16384 + resident_tail,
+                     T=resident_tail, host_ratio=16, layers=1, steps=2, len0=16384 + resident_tail,
                      grow=0, carry_pct=70, zipf_pct=30, third=tg.THIRD_ZIPF)
     ref = GpuWorkload(wl, record=True)
     try:
