@@ -46,6 +46,7 @@ KERNEL_SOURCES = {
     "hs_resolve_kernel_fused": ["hs_resolve.cu", "hs_internal.h"],
     "hs_resolve_layers_kernel": ["hs_resolve.cu", "hs_internal.h"],
     "hs_copy_kernel": ["hs_copy.cu", "hs_internal.h"],
+    "hs_swapin_cluster_kernel": ["hs_resolve.cu", "hs_internal.h"],
 }
 METRIC = "top-k resolves/sec and miss-row GB/s vs measured H2D peak (1xGB300)"
 L2_FLUSH_BYTES = 256 << 20
@@ -289,7 +290,8 @@ def run_ours(args, rank, world, dist):
     from hierarchical_kv_cache_hs_gb300.workload import GpuWorkload
 
     wl = tg.WORKLOADS[args.workload]
-    mode = {"auto": hs.HS_COPY_AUTO, "fused": hs.HS_COPY_FUSED, "split": hs.HS_COPY_SPLIT}[args.copy_mode]
+    mode = {"auto": hs.HS_COPY_AUTO, "fused": hs.HS_COPY_FUSED, "split": hs.HS_COPY_SPLIT,
+            "cluster": hs.HS_COPY_CLUSTER}[args.copy_mode]
     total_steps = PRIME_STEPS + args.warmup + args.steps
     # Several layers: one launch for all of them, or one call per layer.
     one = args.layer_launch == "one" and wl.layers > 1
@@ -313,8 +315,11 @@ def run_ours(args, rank, world, dist):
         w = GpuWorkload(wl, steps=total_steps, record=False, host_trace=want_e2e,
                         request_offset=shard_requests(rank, wl.B)[0], copy_mode=mode)
         stream = torch.cuda.Stream(device=dev)
-        # The library's launch mode for this handle: one kernel (fused) or two.
-        res = {"fused": hs.hs_resolve_launches(w.handles[0].h) == 1}
+        # The library's launch mode for this handle: one kernel (fused, or a
+        # cluster of CTAs per request) or two (split).
+        kind = hs.hs_launch_mode(w.handles[0].h)
+        res = {"fused": kind != hs.HS_COPY_SPLIT, "cluster": kind == hs.HS_COPY_CLUSTER,
+               "cluster_size": hs.hs_cluster_size(w.handles[0].h)}
         try:
             def stats_sum(key):
                 return sum(hs.hs_stats(h.h)[key] for h in w.handles)
@@ -519,8 +524,9 @@ def run_ours(args, rank, world, dist):
         for m in res["misses_per_step"]:
             table = wl.layers * (wl.B * (16 * wl.K + 4 * wl.S)) + 16 * m
             t_roof += max(m * wl.row_bytes / (h2d_peak * 1e9), table / (hbm_gbs * 1e9))
-        kernel = ("hs_resolve_layers_kernel" if one else "hs_resolve_kernel_fused" if fused
-                  else "hs_copy_kernel")
+        cl = res["cluster"] and not one
+        kernel = ("hs_resolve_layers_kernel" if one else "hs_swapin_cluster_kernel" if cl
+                  else "hs_resolve_kernel_fused" if fused else "hs_copy_kernel")
         traffic, host_link, traffic_src = dram_traffic(kernel, wl.name)
         e2e_value = all_units / max_over_ranks(res["e2e_s"]) if "e2e_s" in res else None
         out = {
@@ -535,6 +541,8 @@ def run_ours(args, rank, world, dist):
             "roofline": {"bound": "h2d",
                          "kernel": ("hs_resolve_layers_kernel (every layer's resolve + row fetch, "
                                     "one grid)" if one else
+                                    "hs_swapin_cluster_kernel (resolve + row fetch, a cluster of "
+                                    "%d CTAs per request)" % res["cluster_size"] if cl else
                                     "hs_resolve_kernel<fused> (resolve + row fetch)" if fused
                                     else "hs_copy_kernel"),
                          "achieved": copy_gbs,
@@ -548,8 +556,9 @@ def run_ours(args, rank, world, dist):
                                    if (fused or one) else
                                    {"copy": sum(res["copy_ms"]) / args.steps,
                                     "resolve": sum(res["resolve_ms"]) / args.steps}),
-            "launch_mode": ("fused, all layers in one launch" if one else "fused" if fused
-                            else "split"),
+            "launch_mode": ("fused, all layers in one launch" if one else
+                            "cluster of %d CTAs per request" % res["cluster_size"] if cl else
+                            "fused" if fused else "split"),
             "misses_per_step_mean": statistics.mean(res["misses_per_step"]),
             "inplace_per_step_mean": res["inplace"] / args.steps,
             "e2e": {"value": e2e_value, "unit": "resolves/s",
@@ -803,7 +812,7 @@ def main():
     ap.add_argument("--overlap", action="store_true",
                     help="also time the 4-layer, 128K-context workload with its layers on one "
                          "stream and on one stream per layer")
-    ap.add_argument("--copy-mode", choices=["auto", "fused", "split"], default="auto",
+    ap.add_argument("--copy-mode", choices=["auto", "fused", "split", "cluster"], default="auto",
                     help="launch mode of the step (identical results; see hs_set_copy_mode)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -31,6 +31,7 @@ struct hs_handle {
     int32_t* d_stage_out;
     cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
     int copy_mode;         // HS_COPY_*
+    int cluster_n;         // CTAs per request in cluster mode (1: no cluster fits)
     int policy;            // HS_POLICY_*
     int tail_mode;         // HS_TAIL_*
     int copy_grid;
@@ -121,13 +122,34 @@ bool valid(const hs_handle* h)
     return h != nullptr && h->B > 0;
 }
 
-// The launch mode of a step (HS_COPY_AUTO: by batch size, or by the size of
-// one request's hot buffer, which bounds what a step gives one CTA to copy).
-bool use_fused(const hs_handle* h)
+// The launch of a step: HS_COPY_FUSED, HS_COPY_SPLIT or HS_COPY_CLUSTER.  A
+// cluster mode whose cluster size is 1 runs the fused kernel.  HS_COPY_AUTO:
+// a cluster per request up to HS_CLUSTER_MAX_BATCH requests, else fused;
+// without a cluster size that fits, split below HS_FUSED_MIN_BATCH requests
+// when one request's hot buffer (which bounds what a step gives one CTA to
+// copy) is over HS_FUSED_MAX_REQUEST_BYTES.
+int launch_kind(const hs_handle* h)
 {
-    if (h->copy_mode != HS_COPY_AUTO) return h->copy_mode == HS_COPY_FUSED;
-    return h->B >= HS_FUSED_MIN_BATCH ||
-           (long long)h->S * h->R <= (long long)HS_FUSED_MAX_REQUEST_BYTES;
+    if (h->copy_mode == HS_COPY_CLUSTER)
+        return h->cluster_n >= 2 ? HS_COPY_CLUSTER : HS_COPY_FUSED;
+    if (h->copy_mode != HS_COPY_AUTO) return h->copy_mode;
+    if (h->B <= HS_CLUSTER_MAX_BATCH && h->cluster_n >= 2) return HS_COPY_CLUSTER;
+    return (h->B >= HS_FUSED_MIN_BATCH ||
+            (long long)h->S * h->R <= (long long)HS_FUSED_MAX_REQUEST_BYTES)
+               ? HS_COPY_FUSED
+               : HS_COPY_SPLIT;
+}
+
+// CTAs per request in cluster mode: the largest of 16, 8, 4, 2 with every
+// request's cluster resident at once and no more CTAs than SMs.
+int auto_cluster_size(const hs_handle* h, int sms)
+{
+    const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;
+    for (int n = HS_MAX_CLUSTER; n >= 2; n >>= 1) {
+        if ((long long)h->B * n > sms) continue;
+        if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= h->B) return n;
+    }
+    return 1;
 }
 
 }  // namespace
@@ -220,6 +242,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
     h->copy_mode = HS_COPY_AUTO;
+    h->cluster_n = auto_cluster_size(h, sms);
     h->policy = HS_POLICY_LRU;
     h->tail_mode = HS_TAIL_FIXED;
     const int rc = fill_start_state(h);
@@ -306,12 +329,15 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     const ResolveArgs ra = resolve_args(h, topk_idx, K, out_slot, alias);
 
     const bool prof = h->prof_before && h->prof_after;
-    const bool fused = use_fused(h);
-    if (fused) {
-        // One launch: each request's CTA fetches its own rows.  The profiling
-        // events then bracket the whole step.
+    const int kind = launch_kind(h);
+    if (kind != HS_COPY_SPLIT) {
+        // One launch: each request's CTA (or cluster of CTAs) fetches its own
+        // rows.  The profiling events then bracket the whole step.
         if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
-        if (hs_launch_swapin(ra, h->B, h->copy_unroll, s) != cudaSuccess) return HS_ERR_CUDA;
+        const cudaError_t e = kind == HS_COPY_CLUSTER
+            ? hs_launch_swapin_cluster(ra, h->B, h->cluster_n, h->copy_unroll, s)
+            : hs_launch_swapin(ra, h->B, h->copy_unroll, s);
+        if (e != cudaSuccess) return HS_ERR_CUDA;
         if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
         return HS_OK;
     }
@@ -568,8 +594,34 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
 int hs_resolve_launches(hs_handle* h)
 {
     if (!valid(h)) return HS_ERR_ARG;
-    const bool fused = use_fused(h);
-    return fused ? 1 : 2;
+    return launch_kind(h) == HS_COPY_SPLIT ? 2 : 1;
+}
+
+int hs_launch_mode(hs_handle* h)
+{
+    return valid(h) ? launch_kind(h) : HS_ERR_ARG;
+}
+
+int hs_set_cluster_size(hs_handle* h, int n)
+{
+    if (!valid(h) || n < 0 || n == 1) return HS_ERR_ARG;
+    if (n > HS_MAX_CLUSTER) return HS_ERR_LIMIT;
+    DeviceGuard g(h->device);
+    if (n == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+        h->cluster_n = auto_cluster_size(h, sms > 0 ? sms : 1);
+        return HS_OK;
+    }
+    const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;
+    if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) < 1) return HS_ERR_LIMIT;
+    h->cluster_n = n;
+    return HS_OK;
+}
+
+int hs_cluster_size(hs_handle* h)
+{
+    return valid(h) ? h->cluster_n : HS_ERR_ARG;
 }
 
 int hs_set_tail_mode(hs_handle* h, int mode)
@@ -589,7 +641,7 @@ int hs_set_policy(hs_handle* h, int policy)
 
 int hs_set_copy_mode(hs_handle* h, int mode)
 {
-    if (!valid(h) || mode < HS_COPY_AUTO || mode > HS_COPY_SPLIT) return HS_ERR_ARG;
+    if (!valid(h) || mode < HS_COPY_AUTO || mode > HS_COPY_CLUSTER) return HS_ERR_ARG;
     h->copy_mode = mode;
     return HS_OK;
 }

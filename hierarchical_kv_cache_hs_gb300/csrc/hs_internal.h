@@ -136,6 +136,11 @@ cudaError_t hs_launch_resolve(const ResolveArgs& a, int B, cudaStream_t s);
 cudaError_t hs_launch_swapin(const ResolveArgs& a, int B, int unroll, cudaStream_t s);
 // The same for L handles at once (L * B CTAs).
 cudaError_t hs_launch_swapin_layers(const LayerArgs& p, int L, int unroll, cudaStream_t s);
+// Resolve + row fetch with a cluster of ncl CTAs per request (B * ncl CTAs).
+cudaError_t hs_launch_swapin_cluster(const ResolveArgs& a, int B, int ncl, int unroll,
+                                     cudaStream_t s);
+// Clusters of ncl swap-in CTAs that fit on the device at once (0 if none).
+int hs_cluster_max_active(int K, int S, int ncl, int unroll);
 
 // Copy kernel: `pdl` lets it launch while the resolve grid drains (it waits
 // on the resolve grid's completion before reading the miss lists).

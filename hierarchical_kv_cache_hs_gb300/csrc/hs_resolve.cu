@@ -147,6 +147,68 @@ __device__ __forceinline__ void copy_row_group(const uint8_t* pool_b, uint8_t* b
     }
 }
 
+// ---- thread-block clusters: one request's CTAs on several SMs -------------
+// The miss count of the cluster's resolving CTA, read by the others through
+// distributed shared memory (a file-scope variable has the same offset in
+// every CTA of the kernel).
+__shared__ int s_cluster_m;
+
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_size()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_index()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// Hardware cluster barrier, split into its two halves.  Every thread of every
+// CTA of the cluster arrives once per phase and waits before it arrives
+// again; .release publishes the thread's earlier shared-memory writes to the
+// CTAs that wait (.acquire) on the phase.  (The forms without .aligned: they
+// do not need the warp to be converged where they are called.)
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// The shared-memory address of `p` in CTA `rank` of this cluster.
+__device__ __forceinline__ unsigned cluster_map(const void* p, unsigned rank)
+{
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ int ld_cluster_s32(unsigned addr)
+{
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_cluster_u16(unsigned addr)
+{
+    unsigned short v;
+    asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return (int)v;
+}
+
 // A stamp clamped into [0, step - 1], the range the victim search assumes.
 __device__ __forceinline__ int clamp_stamp(int k, int step)
 {
@@ -178,9 +240,11 @@ __device__ __forceinline__ void write_out(int32_t* g_out, const int (&o)[EMAX], 
 }
 
 // One request's step: CTA `b` of the `nblocks` that serve one handle.
-template <bool FUSED, int U>
+// CLUSTER: this CTA is rank 0 of a cluster of `ncl` CTAs serving request b;
+// the others (cluster_helper) fetch rows from its miss and victim lists.
+template <bool FUSED, int U, bool CLUSTER = false>
 __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
-                                            const unsigned nblocks)
+                                            const unsigned nblocks, const int ncl = 1)
 {
     extern __shared__ __align__(16) int smem[];
     __shared__ int s_w[32];
@@ -411,6 +475,12 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             ++pos;
         }
     }
+    if (CLUSTER) {
+        // Phase 1 of the cluster barrier: the miss list is complete, and the
+        // other CTAs start fetching rows while the victims are chosen.
+        if (tid == 0) s_cluster_m = m;
+        cluster_arrive_release();
+    }
 
     if (m == 0) {
         write_out(g_out, ov, j0, E, K);
@@ -439,7 +509,8 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         uint4 pre[U];
         const int G0 = a.rows_per_group;
         const int cpr0 = a.R >> 4;
-        const bool prefetch = FUSED && G0 * cpr0 <= 32 * U && warp < NW / 2 && m > NW * G0;
+        const bool prefetch = FUSED && !CLUSTER && G0 * cpr0 <= 32 * U && warp < NW / 2 &&
+                              m > NW * G0;
         if (prefetch && warp * G0 < m) {
             const uint8_t* pool_b0 = a.pool + (size_t)b * (size_t)a.H * a.R;
             const int r0 = warp * G0;
@@ -644,7 +715,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 g_mtok[i] = t;
                 g_mslot[i] = v;
             }
-        } else {
+        } else if (!CLUSTER) {
             // ---- (3) table update + host fetch, G rows per warp at a time ----
             const int G = a.rows_per_group;
             const int cpr = a.R >> 4;  // 16-byte chunks per row
@@ -682,6 +753,40 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             }
         }
     }
+    if (CLUSTER) {
+        cluster_wait();            // phase 1 done: every CTA of the cluster is running
+        cluster_arrive_release();  // phase 2: the victims are placed
+        if (m > 0) {
+            // ---- (3) table update for every miss, then this CTA's rows ----
+            for (int i = tid; i < m; i += NT) {
+                const int t = s_mtok[i];
+                const int v = s_vic[i];
+                const int old = s_slot_tok[v];
+                if (old >= 0 && old < a.C) g_tok_slot[old] = -1;
+                else if (old != -1) atomicOr(&s_cnt[2], HS_E_STATE);
+                g_slot_tok[v] = t;
+                g_tok_slot[t] = v;
+                s_stamp[v] = step;
+            }
+            // Row group g (rows [g*G, g*G + G)) belongs to cluster warp g mod
+            // (ncl * NW); this CTA's warps come after the other CTAs'.
+            const int G = a.rows_per_group;
+            const int cpr = a.R >> 4;
+            const uint8_t* pool_b = a.pool + (size_t)b * (size_t)a.H * a.R;
+            uint8_t* buf_b = a.buf + (size_t)b * (size_t)(S + a.T) * a.R;
+            const int ncw = ncl * NW;
+            for (int g = (ncl - 1) * NW + warp; g * G < m; g += ncw) {
+                const int r0 = g * G;
+                long long src = 0, dst = 0;
+                if (lane < G && r0 + lane < m) {
+                    src = (long long)s_mtok[r0 + lane] * a.R;
+                    dst = (long long)s_vic[r0 + lane] * a.R;
+                }
+                copy_row_group<U>(pool_b, buf_b, src, dst, (m - r0) < G ? (m - r0) : G, cpr, lane);
+            }
+        }
+        cluster_wait();            // phase 2 done
+    }
     __syncthreads();
     if (a.fifo) {
         for (int i = tid; i < S; i += NT)
@@ -706,12 +811,102 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             }
         }
     }
+    if (CLUSTER) {
+        // Phase 3: this CTA's lists stay in shared memory until the other
+        // CTAs of the cluster have read them.
+        cluster_arrive_release();
+        cluster_wait();
+    }
+}
+
+// A CTA of rank >= 1 in a request's cluster: it reads the miss list of rank
+// 0 through distributed shared memory as soon as it exists, loads its warps'
+// first row group into registers while rank 0 chooses the victims, and then
+// copies its share of the rows (row group g belongs to cluster warp g mod
+// (ncl * NW), ranks 1.. first).  It writes no table.  The barrier phases
+// match resolve_cta<CLUSTER>: 1 miss list, 2 victims, 3 lists read.
+template <int U>
+__device__ __forceinline__ void cluster_helper(const ResolveArgs& a, const int b, const int rank,
+                                               const int ncl)
+{
+    extern __shared__ __align__(16) int smem[];
+    const int K = a.K, S = a.S;
+    // rank 0's layout (the same dynamic shared memory size in every CTA)
+    int* s_mtok = smem + hs_resolve_region_a_ints(a.hash_bits, K) + 2 * S;
+    uint16_t* s_vic = reinterpret_cast<uint16_t*>(s_mtok + K) + K;
+    const unsigned r_mtok = cluster_map(s_mtok, 0);
+    const unsigned r_vic = cluster_map(s_vic, 0);
+    const unsigned r_m = cluster_map(&s_cluster_m, 0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cw = (rank - 1) * NW + warp;
+    const int ncw = ncl * NW;
+    const int G = a.rows_per_group;
+    const int cpr = a.R >> 4;
+    const uint8_t* pool_b = a.pool + (size_t)b * (size_t)a.H * a.R;
+    uint8_t* buf_b = a.buf + (size_t)b * (size_t)(S + a.T) * a.R;
+
+    cluster_arrive_relaxed();  // phase 1
+    cluster_wait();            // rank 0's miss list is complete
+    const int m = ld_cluster_s32(r_m);
+    // Early fetch: this warp's first group, before the victims are known.
+    uint4 pre[U];
+    const bool early = G * cpr <= 32 * U && cw * G < m;
+    if (early) {
+        const int r0 = cw * G;
+        long long src = 0;
+        if (lane < G && r0 + lane < m) src = (long long)ld_cluster_s32(r_mtok + 4u * (r0 + lane)) * a.R;
+        const int nch = ((m - r0) < G ? (m - r0) : G) * cpr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int cc = u * 32 + lane;
+            const int rr = cc < nch ? cc / cpr : 0;
+            const long long sg = __shfl_sync(FULL, src, rr);
+            if (cc < nch) pre[u] = ld_host_v4(pool_b + sg + ((cc - rr * cpr) << 4));
+        }
+    }
+    cluster_arrive_relaxed();  // phase 2
+    cluster_wait();            // rank 0's victims are placed
+    for (int g = cw; g * G < m; g += ncw) {
+        const int r0 = g * G;
+        long long src = 0, dst = 0;
+        if (lane < G && r0 + lane < m) {
+            src = (long long)ld_cluster_s32(r_mtok + 4u * (r0 + lane)) * a.R;
+            dst = (long long)ld_cluster_u16(r_vic + 2u * (r0 + lane)) * a.R;
+        }
+        const int nrows = (m - r0) < G ? (m - r0) : G;
+        if (early && g == cw) {
+            const int nch = nrows * cpr;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int cc = u * 32 + lane;
+                const int rr = cc < nch ? cc / cpr : 0;
+                const long long dg = __shfl_sync(FULL, dst, rr) + ((cc - rr * cpr) << 4);
+                if (cc < nch) st_v4(buf_b + dg, pre[u]);
+            }
+        } else {
+            copy_row_group<U>(pool_b, buf_b, src, dst, nrows, cpr, lane);
+        }
+    }
+    cluster_arrive_release();  // phase 3: done with rank 0's lists
+    cluster_wait();
 }
 
 template <bool FUSED, int U>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(ResolveArgs a)
 {
     resolve_cta<FUSED, U>(a, blockIdx.x, gridDim.x);
+}
+
+// One cluster of ncl CTAs per request (cluster x serves request x): rank 0
+// resolves and copies a share of the rows, the others fetch the rest.
+template <int U>
+__global__ void __launch_bounds__(NT, 1) hs_swapin_cluster_kernel(ResolveArgs a)
+{
+    const int rank = (int)cluster_rank();
+    const int ncl = (int)cluster_size();
+    const int b = (int)cluster_index();
+    if (rank == 0) resolve_cta<true, U, true>(a, b, gridDim.x / (unsigned)ncl, ncl);
+    else cluster_helper<U>(a, b, rank, ncl);
 }
 
 // Independent layers in one grid: CTA x serves request x mod B of layer
@@ -748,6 +943,18 @@ cudaError_t hs_prepare_resolve()
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(hs_resolve_layers_kernel<8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_swapin_cluster_kernel<9>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_swapin_cluster_kernel<8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_swapin_cluster_kernel<9>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hs_swapin_cluster_kernel<8>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
@@ -792,4 +999,49 @@ cudaError_t hs_launch_swapin_layers(const LayerArgs& p, int L, int unroll, cudaS
     cfg.stream = s;
     if (unroll == 9) return cudaLaunchKernelEx(&cfg, hs_resolve_layers_kernel<9>, p);
     return cudaLaunchKernelEx(&cfg, hs_resolve_layers_kernel<8>, p);
+}
+
+static cudaLaunchConfig_t cluster_config(const ResolveArgs& a, int B, int ncl, cudaStream_t s,
+                                         cudaLaunchAttribute* attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * ncl));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = hs_resolve_smem_bytes(a.K, a.S);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ncl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+cudaError_t hs_launch_swapin_cluster(const ResolveArgs& a, int B, int ncl, int unroll,
+                                     cudaStream_t s)
+{
+    if (!layout_ok(a) || ncl < 2 || ncl > HS_MAX_CLUSTER) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(a, B, ncl, s, attr);
+    if (unroll == 9) return cudaLaunchKernelEx(&cfg, hs_swapin_cluster_kernel<9>, a);
+    return cudaLaunchKernelEx(&cfg, hs_swapin_cluster_kernel<8>, a);
+}
+
+int hs_cluster_max_active(int K, int S, int ncl, int unroll)
+{
+    ResolveArgs a = {};
+    a.K = K;
+    a.S = S;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(a, 1, ncl, nullptr, attr);
+    int n = 0;
+    const cudaError_t e = unroll == 9
+        ? cudaOccupancyMaxActiveClusters(&n, hs_swapin_cluster_kernel<9>, &cfg)
+        : cudaOccupancyMaxActiveClusters(&n, hs_swapin_cluster_kernel<8>, &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }

@@ -41,6 +41,9 @@ HS_POLICY_FIFO = 1
 HS_COPY_AUTO = 0
 HS_COPY_FUSED = 1
 HS_COPY_SPLIT = 2
+HS_COPY_CLUSTER = 3
+HS_MAX_CLUSTER = 16
+HS_CLUSTER_MAX_BATCH = 16
 HS_FUSED_MIN_BATCH = 16
 HS_FUSED_MAX_REQUEST_BYTES = 1 << 20
 
@@ -100,6 +103,9 @@ def _load():
         "hs_h2d_read": ([P, P, Z, I, P], I),
         "hs_profile_events": ([P, P, P], I),
         "hs_set_copy_mode": ([P, I], I),
+        "hs_set_cluster_size": ([P, I], I),
+        "hs_cluster_size": ([P], I),
+        "hs_launch_mode": ([P], I),
         "hs_resolve_launches": ([P], I),
         "hs_set_policy": ([P, I], I),
         "hs_set_tail_mode": ([P, I], I),
@@ -363,6 +369,26 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
 
 def hs_set_copy_mode(h: int, mode: int) -> None:
     _check(lib.hs_set_copy_mode(h, int(mode)), "hs_set_copy_mode")
+
+
+def hs_set_cluster_size(h: int, n: int) -> None:
+    """CTAs per request in cluster mode (0 = the handle's default)."""
+    _check(lib.hs_set_cluster_size(h, int(n)), "hs_set_cluster_size")
+
+
+def hs_cluster_size(h: int) -> int:
+    n = lib.hs_cluster_size(h)
+    if n < 0:
+        raise HsError(n, "hs_cluster_size")
+    return n
+
+
+def hs_launch_mode(h: int) -> int:
+    """HS_COPY_FUSED, HS_COPY_SPLIT or HS_COPY_CLUSTER: what the next hs_resolve launches."""
+    n = lib.hs_launch_mode(h)
+    if n < 0:
+        raise HsError(n, "hs_launch_mode")
+    return n
 
 
 def hs_set_tail_mode(h: int, mode: int) -> None:

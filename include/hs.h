@@ -349,24 +349,37 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
                 hs_stream_t stream);
 
 /*
- * How the step is launched (both give identical results):
- *   HS_COPY_FUSED  one kernel; each request's CTA resolves its row and then
- *                  fetches its own missing rows from the host pool;
- *   HS_COPY_SPLIT  a resolve kernel, then a grid-wide copy kernel over the
- *                  misses of all requests (better when B is small);
- *   HS_COPY_AUTO   fused when B >= HS_FUSED_MIN_BATCH, or when one request's
- *                  hot buffer (S * row_bytes) is at most
- *                  HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
- *                  much to copy; split otherwise (default).  A function of the
- *                  handle alone, so hs_resolve_launches answers per handle.
+ * How the step is launched (all give identical results):
+ *   HS_COPY_FUSED    one kernel; each request's CTA resolves its row and then
+ *                    fetches its own missing rows from the host pool;
+ *   HS_COPY_SPLIT    a resolve kernel, then a grid-wide copy kernel over the
+ *                    misses of all requests;
+ *   HS_COPY_CLUSTER  one kernel with a thread-block cluster of several CTAs
+ *                    per request: the first CTA resolves the row, the others
+ *                    read its miss list from distributed shared memory, load
+ *                    their first rows while it chooses the victims, and the
+ *                    cluster copies the rows together (more SMs per request
+ *                    than FUSED, one launch unlike SPLIT);
+ *   HS_COPY_AUTO     (default) cluster when B <= HS_CLUSTER_MAX_BATCH and a
+ *                    cluster size of 2 or more fits (hs_cluster_size), else
+ *                    fused.  Without such a cluster size: fused when
+ *                    B >= HS_FUSED_MIN_BATCH, or when one request's hot
+ *                    buffer (S * row_bytes) is at most
+ *                    HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
+ *                    much to copy; split otherwise.  A function of the handle
+ *                    alone, so hs_resolve_launches answers per handle.
  * Source: HiSparse blog, "効率的なSwap-inカーネル" (one dedicated kernel does
- * steps (1)-(3)); the split form is this library's, with no passage.
+ * steps (1)-(3)); the split and cluster forms are this library's, with no
+ * passage.
  */
-#define HS_COPY_AUTO   0
-#define HS_COPY_FUSED  1
-#define HS_COPY_SPLIT  2
+#define HS_COPY_AUTO     0
+#define HS_COPY_FUSED    1
+#define HS_COPY_SPLIT    2
+#define HS_COPY_CLUSTER  3
 #define HS_FUSED_MIN_BATCH 16
 #define HS_FUSED_MAX_REQUEST_BYTES (1 << 20)
+#define HS_MAX_CLUSTER   16
+#define HS_CLUSTER_MAX_BATCH 16
 int hs_set_copy_mode(hs_handle* h, int mode);
 
 /*
@@ -404,7 +417,24 @@ int hs_set_policy(hs_handle* h, int policy);
 #define HS_TAIL_SLIDING  1
 int hs_set_tail_mode(hs_handle* h, int mode);
 
-/* Kernel launches one hs_resolve makes on this handle (1 fused, 2 split), or HS_ERR_ARG.
+/*
+ * CTAs per request in HS_COPY_CLUSTER mode.  n = 0 (the default) picks the
+ * largest of 16, 8, 4, 2 for which all B clusters run at once on the device
+ * with B * n no larger than its SM count; otherwise 2 <= n <= HS_MAX_CLUSTER,
+ * refused (HS_ERR_LIMIT) when the device cannot run clusters of n such CTAs.
+ * hs_cluster_size returns the size in use (1 when no cluster size fits: the
+ * cluster mode then launches the fused kernel).
+ * Source: no passage (a launch-shape knob of this library).
+ */
+int hs_set_cluster_size(hs_handle* h, int n);
+int hs_cluster_size(hs_handle* h);
+
+/* The launch the next hs_resolve on this handle makes: HS_COPY_FUSED,
+ * HS_COPY_SPLIT or HS_COPY_CLUSTER (never HS_COPY_AUTO), or HS_ERR_ARG.
+ * Source: no passage (a measurement aid). */
+int hs_launch_mode(hs_handle* h);
+
+/* Kernel launches one hs_resolve makes on this handle (1 fused or cluster, 2 split), or HS_ERR_ARG.
  * Source: no passage (a measurement aid). */
 int hs_resolve_launches(hs_handle* h);
 

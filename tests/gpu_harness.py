@@ -21,12 +21,27 @@ class GpuResult:
     pass
 
 
+def set_cluster_size(h, n):
+    """Cluster-mode CTAs per request; a size the device cannot run falls back to 8."""
+    try:
+        hs.hs_set_cluster_size(h, n)
+    except hs.HsError as e:
+        if e.code != hs.HS_ERR_LIMIT or n <= 8:
+            raise
+        hs.hs_set_cluster_size(h, 8)
+
+
 def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO,
-            policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False, one_launch=False):
+            policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False, one_launch=False,
+            cluster_size=0):
     """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one.
 
-    ``policy`` is one eviction policy for every layer, or a list with one per layer."""
+    ``policy`` is one eviction policy for every layer, or a list with one per layer.
+    ``cluster_size``: CTAs per request in cluster mode (0 = the handle's default)."""
     w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
+    if cluster_size:
+        for h in w.handles:
+            set_cluster_size(h.h, cluster_size)
     for layer, h in enumerate(w.handles):
         hs.hs_set_policy(h.h, policy[layer] if isinstance(policy, (list, tuple)) else policy)
     res_policy = policy

@@ -28,9 +28,10 @@ def _built():
 
 
 def _run_and_compare(wl, steps=None, requests=None, graph=False, trace=None, expect_err=0,
-                     copy_mode=0, policy=0):
+                     copy_mode=0, policy=0, cluster_size=0):
     from gpu_harness import check_counters, compare, gpu_run
-    res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode, policy=policy)
+    res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode, policy=policy,
+                  cluster_size=cluster_size)
     try:
         tot, err = compare(wl, res, requests=requests)
         if requests is None:
@@ -219,6 +220,26 @@ def test_parity_wide_random(seed):
 
 
 @pytest.mark.parametrize("seed", range(12))
+def test_parity_wide_random_cluster(seed):
+    """The wide random workloads in cluster mode (several CTAs per request),
+    with a random cluster size."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _wide_workload(500 + seed)
+    rng = random.Random(9500 + seed)
+    pol = [rng.choice([0, 1]) for _ in range(wl.layers)]
+    n = rng.choice([0, 2, 3, 4, 8, 16])
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, copy_mode=hs.HS_COPY_CLUSTER, policy=pol, cluster_size=n)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+    finally:
+        res.workload.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
 def test_parity_random_multi_position(seed):
     """Seeded random draft-position steps: P rows per request that repeat one
     another's tokens and carry padding, random sizes, launch mode and policy."""
@@ -249,6 +270,8 @@ def test_parity_random_multi_position(seed):
     h = hs.Handle(B, C, R, S, ratio, 0)
     try:
         hs.hs_set_copy_mode(h.h, rng.choice([0, 1, 2]))
+        if seed % 3 == 2:  # a third of the seeds in cluster mode
+            hs.hs_set_copy_mode(h.h, hs.HS_COPY_CLUSTER)
         hs.hs_set_policy(h.h, policy)
         pool = h.host_pool()
         for b in range(B):
@@ -303,7 +326,27 @@ def test_parity_random_workloads(seed):
         res.workload.close()
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(32))
+def test_parity_random_workloads_cluster(seed):
+    """The random workloads in cluster mode with a random cluster size (0 is
+    the handle's default), every request of every layer against the oracle."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _random_workload(600 + seed)
+    rng = random.Random(1600 + seed)
+    policies = [rng.choice([0, 1]) for _ in range(wl.layers)]
+    n = rng.choice([0, 0, 2, 3, 4, 5, 8, 16])
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, copy_mode=hs.HS_COPY_CLUSTER, policy=policies, cluster_size=n)
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+    finally:
+        res.workload.close()
+
+
+@pytest.mark.parametrize("seed", range(24))
 def test_parity_random_noisy_traces(seed):
     """The random workloads with input errors mixed into every row: padding,
     indices below -1 or past the current length, and repeats of an earlier
@@ -326,9 +369,13 @@ def test_parity_random_noisy_traces(seed):
         idx = np.nonzero(rep)
         trace[idx] = trace[idx[:-1] + (nrng.integers(0, idx[-1]),)] if len(idx[-1]) else trace[idx]
     expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
-    res = gpu_run(wl, trace=trace, copy_mode=rng.choice([0, 1, 2]),
-                  policy=[rng.choice([0, 1]) for _ in range(wl.layers)],
-                  one_launch=wl.layers > 1 and rng.random() < 0.5)
+    mode = rng.choice([0, 1, 2])
+    policy = [rng.choice([0, 1]) for _ in range(wl.layers)]
+    one = wl.layers > 1 and rng.random() < 0.5
+    if seed >= 16:  # the same kind of traces in cluster mode
+        mode, one = hs.HS_COPY_CLUSTER, False
+    res = gpu_run(wl, trace=trace, copy_mode=mode, policy=policy, one_launch=one,
+                  cluster_size=[0, 2, 4, 8][seed % 4] if seed >= 16 else 0)
     try:
         tot, err = compare(wl, res)
         check_counters(wl, res, tot, err | expect)
@@ -385,7 +432,7 @@ def test_noalloc_random_matches_handle_path(seed):
         ref.close()
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", list(range(12)) + [12, 15, 18, 21])
 def test_parity_random_entry_points(seed):
     """Random workloads through the other entry points: the whole run replayed
     from one CUDA graph, the copy-engine variant, or host buffers (against the
@@ -400,8 +447,11 @@ def test_parity_random_entry_points(seed):
     expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
     kind = seed % 3
     if kind < 2:
+        mode = rng.choice([0, 1, 2])
+        if kind == 0 and seed >= 12:
+            mode, one = hs.HS_COPY_CLUSTER, False  # graph replay in cluster mode
         res = gpu_run(wl, graph=kind == 0, copy_engine=kind == 1, one_launch=one and kind == 0,
-                      copy_mode=rng.choice([0, 1, 2]))
+                      copy_mode=mode, cluster_size=[0, 2, 4, 8][seed % 4] if mode == 3 else 0)
         try:
             tot, err = compare(wl, res)
             check_counters(wl, res, tot, err | expect)
@@ -563,12 +613,21 @@ def test_parity_edge_sizes(name):
     _run_and_compare(EDGE[name])
 
 
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_parity_edge_sizes_cluster(name):
+    """The edge sizes with a cluster of CTAs per request (4, or the default)."""
+    from hierarchical_kv_cache_hs_gb300 import hs
+    _run_and_compare(EDGE[name], copy_mode=hs.HS_COPY_CLUSTER, cluster_size=4)
+    if EDGE[name].B <= 32:
+        _run_and_compare(EDGE[name], steps=min(EDGE[name].steps, 10), copy_mode=hs.HS_COPY_CLUSTER)
+
+
 SLIDE = tg.Workload("slide_b16_c8k_tail256", 89, B=16, C=8192, K=512, S=1024, T=256,
                     host_ratio=8, layers=1, steps=600, len0=4096, grow=1, carry_pct=60,
                     zipf_pct=30, third=tg.THIRD_RECENT, recent=1024, sliding=True)
 
 
-@pytest.mark.parametrize("mode,policy", [(0, 0), (2, 0), (1, 1)])
+@pytest.mark.parametrize("mode,policy", [(0, 0), (2, 0), (1, 1), (3, 0), (3, 1)])
 def test_parity_sliding_tail(mode, policy):
     """A sliding tail: tokens that leave it are written back to the host pool
     and later come back through the hot buffer as ordinary misses."""
@@ -628,7 +687,7 @@ def test_parity_invalid_and_padding():
     assert (res.out[0, 3] == -1).all() and (res.misses[0, 3] == 0).all()
 
 
-@pytest.mark.parametrize("mode", [1, 2], ids=["fused", "split"])
+@pytest.mark.parametrize("mode", [1, 2, 3], ids=["fused", "split", "cluster"])
 def test_graph_replay_matches_oracle(mode):
     """The whole step sequence captured in one CUDA graph and replayed."""
     for name in ("tiny_b1_c8k", "b32_c32k_s4096"):
@@ -640,7 +699,10 @@ def test_graph_replay_matches_oracle(mode):
 
 @pytest.mark.parametrize("name,mode", [("tiny_b1_c8k", 1), ("b32_c32k_s4096", 2),
                                        ("b64_c64k_s4096", 2), ("ragged", 1),
-                                       ("max_sizes", 1), ("single_slot", 1)])
+                                       ("max_sizes", 1), ("single_slot", 1),
+                                       ("tiny_b1_c8k", 3), ("b32_c32k_s4096", 3),
+                                       ("b64_c64k_s4096", 3), ("b64_c64k_s2048", 3),
+                                       ("b256_c32k_grow_tail512", 3)])
 def test_parity_other_launch_mode(name, mode):
     """The launch mode that the default (fused from 16 requests up) does not pick."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
@@ -649,7 +711,8 @@ def test_parity_other_launch_mode(name, mode):
 
 @pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 2),
                                        ("tiny_b1_c8k", 0), ("b256_c32k_grow_tail512", 0),
-                                       ("ragged", 1), ("odd_k", 1), ("odd_k", 2)])
+                                       ("ragged", 1), ("odd_k", 1), ("odd_k", 2),
+                                       ("b32_c32k_s4096", 3), ("odd_k", 3)])
 def test_parity_fifo_policy(name, mode):
     """FIFO eviction (hits keep their fill stamp) against the oracle's FIFO."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
@@ -678,7 +741,7 @@ def test_parity_copy_engine_variant(name):
         res.workload.close()
 
 
-@pytest.mark.parametrize("mode", [1, 2], ids=["fused", "split"])
+@pytest.mark.parametrize("mode", [1, 2, 3], ids=["fused", "split", "cluster"])
 def test_parity_multi_position(mode):
     """Two draft positions per step: the second row repeats about half of the
     first's tokens; repeats share their first occurrence's slot."""
@@ -989,3 +1052,35 @@ def test_device_errors_leave_context_usable():
         assert st["misses"] == 128 and st["steps"] == 1 and st["err_bits"] == 0
     finally:
         h.close()
+
+
+def test_cluster_size_settings():
+    """hs_set_cluster_size: 0 picks the default, 2..HS_MAX_CLUSTER are taken
+    when the device runs them, other values are refused; cluster mode is one
+    launch per step."""
+    from hierarchical_kv_cache_hs_gb300 import hs
+    h = hs.Handle(4, 8192, 1152, 1024, 8)
+    try:
+        auto = hs.hs_cluster_size(h.h)
+        assert auto in (1, 2, 4, 8, 16)
+        assert auto >= 2  # 4 requests leave most SMs idle
+        with pytest.raises(hs.HsError):
+            hs.hs_set_cluster_size(h.h, 1)
+        with pytest.raises(hs.HsError):
+            hs.hs_set_cluster_size(h.h, -1)
+        with pytest.raises(hs.HsError):
+            hs.hs_set_cluster_size(h.h, hs.HS_MAX_CLUSTER + 1)
+        for n in (2, 3, 8):
+            hs.hs_set_cluster_size(h.h, n)
+            assert hs.hs_cluster_size(h.h) == n
+        hs.hs_set_cluster_size(h.h, 0)
+        assert hs.hs_cluster_size(h.h) == auto
+        hs.hs_set_copy_mode(h.h, hs.HS_COPY_CLUSTER)
+        assert hs.hs_resolve_launches(h.h) == 1
+    finally:
+        h.close()
+    big = hs.Handle(200, 4096, 64, 256, 16)
+    try:
+        assert hs.hs_cluster_size(big.h) == 1  # 200 requests fill the SMs already
+    finally:
+        big.close()

@@ -52,7 +52,7 @@ def _rows(rng, st_tok_slot, cold, C, K, hit_frac):
 
 
 @pytest.mark.parametrize("policy", [0, 1], ids=["lru", "fifo"])
-@pytest.mark.parametrize("mode", [1, 2], ids=["fused", "split"])
+@pytest.mark.parametrize("mode", [1, 2, 3], ids=["fused", "split", "cluster"])
 @pytest.mark.parametrize("step0,old_frac", [(5000, 0.5), (5000, 0.03), (100000, 0.6),
                                             ((1 << 30) + 12345, 0.7), (700, 0.5)])
 def test_resume_matches_oracle(mode, step0, old_frac, policy):
