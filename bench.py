@@ -593,6 +593,9 @@ def run_ours(args, rank, world, dist):
     line["wall_s_timed_region"] = main["wall_s"]
     line["step_ms_quantiles"] = _quantiles(main["step_ms"])
     line["context"] = CONTEXT
+    line["setup"] = ("each host pool is filled, then read once by the GPU (hs_h2d_read) before "
+                     "the first step, as a long-lived serving pool is warm; the first 10 trace "
+                     "steps and the warm-up steps run untimed")
     if args.overlap and rank == 0:
         line["layer_overlap"] = layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev)
     if "ce_s" in main:

@@ -124,31 +124,36 @@ bool valid(const hs_handle* h)
 
 // The launch of a step: HS_COPY_FUSED, HS_COPY_SPLIT or HS_COPY_CLUSTER.  A
 // cluster mode whose cluster size is 1 runs the fused kernel.  HS_COPY_AUTO:
-// a cluster per request up to HS_CLUSTER_MAX_BATCH requests, else fused;
-// without a cluster size that fits, split below HS_FUSED_MIN_BATCH requests
-// when one request's hot buffer (which bounds what a step gives one CTA to
-// copy) is over HS_FUSED_MAX_REQUEST_BYTES.
+// a cluster per request whenever a cluster size of 2 or more runs on the
+// device; otherwise fused, or split below HS_FUSED_MIN_BATCH requests when
+// one request's hot buffer (which bounds what a step gives one CTA to copy)
+// is over HS_FUSED_MAX_REQUEST_BYTES.
 int launch_kind(const hs_handle* h)
 {
     if (h->copy_mode == HS_COPY_CLUSTER)
         return h->cluster_n >= 2 ? HS_COPY_CLUSTER : HS_COPY_FUSED;
     if (h->copy_mode != HS_COPY_AUTO) return h->copy_mode;
-    if (h->B <= HS_CLUSTER_MAX_BATCH && h->cluster_n >= 2) return HS_COPY_CLUSTER;
+    if (h->cluster_n >= 2) return HS_COPY_CLUSTER;
     return (h->B >= HS_FUSED_MIN_BATCH ||
             (long long)h->S * h->R <= (long long)HS_FUSED_MAX_REQUEST_BYTES)
                ? HS_COPY_FUSED
                : HS_COPY_SPLIT;
 }
 
-// CTAs per request in cluster mode: the largest of 16, 8, 4, 2 with every
-// request's cluster resident at once and no more CTAs than SMs.
-int auto_cluster_size(const hs_handle* h, int sms)
+// CTAs per request in cluster mode (measured on GB300, 1-256 requests of
+// 2048-of-4096 slots): 16 up to HS_CLUSTER_WIDE_BATCH requests, when all of
+// their clusters run at once (8 when 16 do not fit), else 4; each size falls
+// back to the next smaller one the device cannot run.  Above 4 requests,
+// clusters of 4 were the fastest at every batch size measured, also past one
+// wave of the SMs: later clusters resolve while earlier ones copy.
+int auto_cluster_size(const hs_handle* h)
 {
     const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;
-    for (int n = HS_MAX_CLUSTER; n >= 2; n >>= 1) {
-        if ((long long)h->B * n > sms) continue;
-        if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= h->B) return n;
-    }
+    if (h->B <= HS_CLUSTER_WIDE_BATCH)
+        for (int n = HS_MAX_CLUSTER; n > 4; n >>= 1)
+            if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= h->B) return n;
+    for (int n = 4; n >= 2; n >>= 1)
+        if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= 1) return n;
     return 1;
 }
 
@@ -242,7 +247,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
     h->copy_mode = HS_COPY_AUTO;
-    h->cluster_n = auto_cluster_size(h, sms);
+    h->cluster_n = auto_cluster_size(h);
     h->policy = HS_POLICY_LRU;
     h->tail_mode = HS_TAIL_FIXED;
     const int rc = fill_start_state(h);
@@ -608,9 +613,7 @@ int hs_set_cluster_size(hs_handle* h, int n)
     if (n > HS_MAX_CLUSTER) return HS_ERR_LIMIT;
     DeviceGuard g(h->device);
     if (n == 0) {
-        int sms = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
-        h->cluster_n = auto_cluster_size(h, sms > 0 ? sms : 1);
+        h->cluster_n = auto_cluster_size(h);
         return HS_OK;
     }
     const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;

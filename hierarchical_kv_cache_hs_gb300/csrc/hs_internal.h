@@ -105,14 +105,16 @@ __host__ __device__ inline int hs_hash_bits(int K)
 // Ints of the region shared by the dedup hash (2 << hash_bits) in phase 1 and,
 // once the miss list exists, the age histograms (HS_AGE_SUBHIST * HS_AGE_BINS)
 // followed by the out_slot values, entry e of thread tid at e * threads + tid
-// (ceil(K / threads) * threads ints).  From K = 1025 on the hash alone is
-// larger than both.  A multiple of 4 ints, so that the stamp row after it
-// starts on the 16-byte boundary its asynchronous copies and int4 reads need.
+// (ceil(K / threads) * threads ints), and the cluster kernel's copy list
+// (uint16 [K]).  From K = 1025 on the hash alone is larger than all of them.
+// A multiple of 4 ints, so that the stamp row after it starts on the 16-byte
+// boundary its asynchronous copies and int4 reads need.
 __host__ __device__ inline int hs_resolve_region_a_ints(int hash_bits, int K)
 {
     const int hc2 = 2 << hash_bits;
     const int per_thread = (K + HS_RESOLVE_THREADS - 1) / HS_RESOLVE_THREADS;
-    const int later = (HS_AGE_SUBHIST * HS_AGE_BINS + per_thread * HS_RESOLVE_THREADS + 3) & ~3;
+    const int later =
+        (HS_AGE_SUBHIST * HS_AGE_BINS + per_thread * HS_RESOLVE_THREADS + (K + 1) / 2 + 3) & ~3;
     return hc2 > later ? hc2 : later;
 }
 

@@ -148,10 +148,10 @@ __device__ __forceinline__ void copy_row_group(const uint8_t* pool_b, uint8_t* b
 }
 
 // ---- thread-block clusters: one request's CTAs on several SMs -------------
-// The miss count of the cluster's resolving CTA, read by the others through
-// distributed shared memory (a file-scope variable has the same offset in
-// every CTA of the kernel).
-__shared__ int s_cluster_m;
+// The copy-list length of the cluster's resolving CTA, read by the others
+// through distributed shared memory (a file-scope variable has the same
+// offset in every CTA of the kernel).
+__shared__ int s_cluster_mc;  // misses on the copy list (not fetched ahead)
 
 __device__ __forceinline__ unsigned cluster_rank()
 {
@@ -213,6 +213,38 @@ __device__ __forceinline__ int ld_cluster_u16(unsigned addr)
 __device__ __forceinline__ int clamp_stamp(int k, int step)
 {
     return k < 0 ? 0 : (k >= step ? step - 1 : k);
+}
+
+// One thread's top-k entries [j0, j0 + E) (entries at or past K read as -1),
+// as 16-byte (else 8-byte) loads where the run is whole and aligned: the row
+// may be mapped host memory, where each 4-byte load of a warp would move its
+// own sectors across the host link.
+__device__ __forceinline__ void load_row(int (&tk)[EMAX], const int32_t* g_row, int j0, int E,
+                                         int K)
+{
+    const int32_t* src = g_row + j0;
+    if (j0 + E <= K && (E & 3) == 0 && ((uintptr_t)src & 15u) == 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; e += 4) {
+            int4 v = make_int4(-1, -1, -1, -1);
+            if (e < E) v = *reinterpret_cast<const int4*>(src + e);
+            tk[e] = v.x;
+            tk[e + 1] = v.y;
+            tk[e + 2] = v.z;
+            tk[e + 3] = v.w;
+        }
+    } else if (j0 + E <= K && (E & 1) == 0 && ((uintptr_t)src & 7u) == 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; e += 2) {
+            int2 v = make_int2(-1, -1);
+            if (e < E) v = *reinterpret_cast<const int2*>(src + e);
+            tk[e] = v.x;
+            tk[e + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) tk[e] = (e < E && j0 + e < K) ? src[e] : -1;
+    }
 }
 
 // One thread's out_slot entries [j0, j0 + E) that lie below K, written with
@@ -299,8 +331,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     const int E = (K + NT - 1) / NT;
     const int j0 = tid * E;
     int tk[EMAX];
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) tk[e] = (e < E && j0 + e < K) ? g_topk[j0 + e] : -1;
+    load_row(tk, g_topk, j0, E, K);
     // The two S-entry rows go to shared memory with asynchronous 16-byte
     // copies when they are 16-byte aligned, so all of them are in flight at
     // once; otherwise with plain loads.
@@ -379,6 +410,31 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     if (tid < 3) s_cnt[tid] = 0;
     __syncthreads();
 
+    // Cluster: the other CTAs fetch rows ahead of the miss list.  They rank the
+    // candidate misses of each warp's entries -- valid cold tokens outside the
+    // buffer, repeats included -- in row order, and the first (ncl - 1) * G of
+    // each warp are theirs.  This CTA ranks them the same way, so each miss
+    // either was fetched ahead or goes on the copy list, never both.
+    unsigned pfmask = 0;
+    if (CLUSTER) {
+        const int PF = (a.rows_per_group * (a.R >> 4) <= 32 * U) ? (ncl - 1) * a.rows_per_group : 0;
+        unsigned cmask = 0;
+        int c = 0;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if (cl[e] == C_MISS && tk[e] < cold && (sl[e] < 0 || sl[e] >= S)) {
+                cmask |= 1u << e;
+                ++c;
+            }
+        int q = warp_incl_scan(c, lane) - c;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if ((cmask >> e) & 1u) {
+                if (q < PF) pfmask |= 1u << e;
+                ++q;
+            }
+    }
+
     // Repeated indices: the first occurrence in row order wins.  A resident
     // token claims its slot by raising the slot's stamp word to
     // step + K - j (the largest value belongs to the smallest j); every other
@@ -407,7 +463,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         }
     }
     __syncthreads();
-    int nh = 0, ni = 0, nm = 0;
+    int nh = 0, ni = 0, nm = 0, nmc = 0;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         const int j = j0 + e;
@@ -450,6 +506,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 ++ni;
             } else {
                 ++nm;
+                if (!((pfmask >> e) & 1u)) ++nmc;
             }
         } else {
             ov[e] = -1;
@@ -464,21 +521,36 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         if (err) atomicOr(&s_cnt[2], err);
     }
 
-    int m = 0;
-    int pos = block_excl_scan(nm, s_w, &m);
+    int m = 0, mc = 0, pos, pos2 = 0;
+    if (CLUSTER) {
+        // Both scans at once: misses, and misses not fetched ahead (counts
+        // below 2^16).
+        int tot;
+        const int packed = block_excl_scan((nm << 16) | nmc, s_w, &tot);
+        pos = packed >> 16;
+        pos2 = packed & 0xffff;
+        m = tot >> 16;
+        mc = tot & 0xffff;
+    } else {
+        pos = block_excl_scan(nm, s_w, &m);
+    }
+    // The copy list (cluster only): the indices of the misses not fetched
+    // ahead, in the hash's region, which the scan's barriers have retired.
+    uint16_t* s_clist = reinterpret_cast<uint16_t*>(s_out + E * NT);
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         if (cl[e] == C_MISS) {
             s_mtok[pos] = tk[e];
             s_mj[pos] = (uint16_t)(j0 + e);
             ov[e] = -(2 + pos);
+            if (CLUSTER && !((pfmask >> e) & 1u)) s_clist[pos2++] = (uint16_t)pos;
             ++pos;
         }
     }
     if (CLUSTER) {
-        // Phase 1 of the cluster barrier: the miss list is complete, and the
-        // other CTAs start fetching rows while the victims are chosen.
-        if (tid == 0) s_cluster_m = m;
+        // Phase 1 of the cluster barrier: the miss list and the copy list are
+        // complete.
+        if (tid == 0) s_cluster_mc = mc;
         cluster_arrive_release();
     }
 
@@ -693,6 +765,10 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                     o = i < m ? (int)s_vic[i] : -1;
                 }
                 fo[e] = o;
+                // Cluster: the final slots replace the miss indices, for the
+                // CTAs whose rows were fetched ahead (each thread rewrites only
+                // its own entries).
+                if (CLUSTER && e < E) s_out[e * NT + tid] = o;
             }
             write_out(g_out, fo, j0, E, K);
         }
@@ -754,7 +830,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         }
     }
     if (CLUSTER) {
-        cluster_wait();            // phase 1 done: every CTA of the cluster is running
+        cluster_wait();            // phase 1 done: the other CTAs have read the page table
         cluster_arrive_release();  // phase 2: the victims are placed
         if (m > 0) {
             // ---- (3) table update for every miss, then this CTA's rows ----
@@ -768,21 +844,23 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 g_tok_slot[t] = v;
                 s_stamp[v] = step;
             }
-            // Row group g (rows [g*G, g*G + G)) belongs to cluster warp g mod
-            // (ncl * NW); this CTA's warps come after the other CTAs'.
+            // Row group g of the copy list (entries [g*G, g*G + G)) belongs
+            // to cluster warp g mod (ncl * NW); this CTA's warps come after
+            // the other CTAs'.
             const int G = a.rows_per_group;
             const int cpr = a.R >> 4;
             const uint8_t* pool_b = a.pool + (size_t)b * (size_t)a.H * a.R;
             uint8_t* buf_b = a.buf + (size_t)b * (size_t)(S + a.T) * a.R;
             const int ncw = ncl * NW;
-            for (int g = (ncl - 1) * NW + warp; g * G < m; g += ncw) {
+            for (int g = (ncl - 1) * NW + warp; g * G < mc; g += ncw) {
                 const int r0 = g * G;
                 long long src = 0, dst = 0;
-                if (lane < G && r0 + lane < m) {
-                    src = (long long)s_mtok[r0 + lane] * a.R;
-                    dst = (long long)s_vic[r0 + lane] * a.R;
+                if (lane < G && r0 + lane < mc) {
+                    const int i = s_clist[r0 + lane];
+                    src = (long long)s_mtok[i] * a.R;
+                    dst = (long long)s_vic[i] * a.R;
                 }
-                copy_row_group<U>(pool_b, buf_b, src, dst, (m - r0) < G ? (m - r0) : G, cpr, lane);
+                copy_row_group<U>(pool_b, buf_b, src, dst, (mc - r0) < G ? (mc - r0) : G, cpr, lane);
             }
         }
         cluster_wait();            // phase 2 done
@@ -819,43 +897,98 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
     }
 }
 
-// A CTA of rank >= 1 in a request's cluster: it reads the miss list of rank
-// 0 through distributed shared memory as soon as it exists, loads its warps'
-// first row group into registers while rank 0 chooses the victims, and then
-// copies its share of the rows (row group g belongs to cluster warp g mod
-// (ncl * NW), ranks 1.. first).  It writes no table.  The barrier phases
-// match resolve_cta<CLUSTER>: 1 miss list, 2 victims, 3 lists read.
+// A CTA of rank >= 1 in a request's cluster.  Before rank 0 has its miss
+// list, it loads the top-k row and gathers the page table itself, ranks each
+// warp's candidate misses as rank 0 does (valid cold tokens outside the
+// buffer, in row order), and its warp w loads candidates
+// [(rank - 1) * G, rank * G) of warp w's entries into registers.  Once rank
+// 0 has placed the victims, each of those rows that is a miss goes to its
+// victim slot (rank 0's out values in shared memory give its miss index), and
+// the CTA copies its share of the rows on rank 0's copy list (group g to
+// cluster warp g mod (ncl * NW), ranks 1.. first).  It writes no table.  The
+// barrier phases match resolve_cta<CLUSTER>: 1 page table read / miss lists
+// built, 2 victims placed, 3 lists read.
 template <int U>
 __device__ __forceinline__ void cluster_helper(const ResolveArgs& a, const int b, const int rank,
                                                const int ncl)
 {
     extern __shared__ __align__(16) int smem[];
     const int K = a.K, S = a.S;
+    const int E = (K + NT - 1) / NT;
     // rank 0's layout (the same dynamic shared memory size in every CTA)
+    int* s_out = smem + NSUB * NB;
+    uint16_t* s_clist = reinterpret_cast<uint16_t*>(s_out + E * NT);
     int* s_mtok = smem + hs_resolve_region_a_ints(a.hash_bits, K) + 2 * S;
     uint16_t* s_vic = reinterpret_cast<uint16_t*>(s_mtok + K) + K;
+    const unsigned r_out = cluster_map(s_out, 0);
+    const unsigned r_clist = cluster_map(s_clist, 0);
     const unsigned r_mtok = cluster_map(s_mtok, 0);
     const unsigned r_vic = cluster_map(s_vic, 0);
-    const unsigned r_m = cluster_map(&s_cluster_m, 0);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cw = (rank - 1) * NW + warp;
-    const int ncw = ncl * NW;
+    const unsigned r_mc = cluster_map(&s_cluster_mc, 0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = a.rows_per_group;
     const int cpr = a.R >> 4;
+    const int ncw = ncl * NW;
     const uint8_t* pool_b = a.pool + (size_t)b * (size_t)a.H * a.R;
     uint8_t* buf_b = a.buf + (size_t)b * (size_t)(S + a.T) * a.R;
+    // This CTA's own shared memory: the rows its warps fetch ahead, [NW][G]
+    // tokens and [NW][G] row positions.
+    int* s_pf_tok = smem;
+    int* s_pf_j = smem + NW * G;
 
-    cluster_arrive_relaxed();  // phase 1
-    cluster_wait();            // rank 0's miss list is complete
-    const int m = ld_cluster_s32(r_m);
-    // Early fetch: this warp's first group, before the victims are known.
+    // ---- fetch ahead: this CTA's candidates, ranked as rank 0 ranks them ----
+    const int len = a.len[b];
+    const int cold = a.sliding ? (len - a.T > 0 ? len - a.T : 0) : a.cold;
+    const int32_t* g_topk = a.topk + (size_t)b * K;
+    const int32_t* g_tok_slot = a.tok_slot + (size_t)b * a.C;
+    const int j0 = tid * E;
+    int tk[EMAX], sl[EMAX];
+    load_row(tk, g_topk, j0, E, K);
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int t = tk[e];
+        sl[e] = -1;
+        if (t >= 0 && t < len && t < a.C && t < cold) sl[e] = g_tok_slot[t];
+    }
+    const bool fits = G * cpr <= 32 * U;  // a row group fits the registers
+    const int lo = (rank - 1) * G;
+    unsigned cmask = 0;
+    int c = 0;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int t = tk[e];
+        if (t >= 0 && t < len && t < a.C && t < cold && (sl[e] < 0 || sl[e] >= S)) {
+            cmask |= 1u << e;
+            ++c;
+        }
+    }
+    const int incl = warp_incl_scan(c, lane);
+    int q = incl - c;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+        if ((cmask >> e) & 1u) {
+            if (fits && q >= lo && q < lo + G) {
+                s_pf_tok[warp * G + (q - lo)] = tk[e];
+                s_pf_j[warp * G + (q - lo)] = j0 + e;
+            }
+            ++q;
+        }
+    const int wtot = __shfl_sync(FULL, incl, 31);
+    const int np = fits ? (wtot - lo < 0 ? 0 : (wtot - lo > G ? G : wtot - lo)) : 0;
+    // Phase 1: this CTA's page-table reads are done (their values are in
+    // use), so rank 0 may update the tables; the loads below may then wait
+    // for room in this SM's memory path without holding rank 0 up.
+    cluster_arrive_release();
+    __syncwarp();
     uint4 pre[U];
-    const bool early = G * cpr <= 32 * U && cw * G < m;
-    if (early) {
-        const int r0 = cw * G;
+    int jr = 0;
+    const int nch = np * cpr;
+    if (np > 0) {
         long long src = 0;
-        if (lane < G && r0 + lane < m) src = (long long)ld_cluster_s32(r_mtok + 4u * (r0 + lane)) * a.R;
-        const int nch = ((m - r0) < G ? (m - r0) : G) * cpr;
+        if (lane < np) {
+            src = (long long)s_pf_tok[warp * G + lane] * a.R;
+            jr = s_pf_j[warp * G + lane];
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int cc = u * 32 + lane;
@@ -864,28 +997,41 @@ __device__ __forceinline__ void cluster_helper(const ResolveArgs& a, const int b
             if (cc < nch) pre[u] = ld_host_v4(pool_b + sg + ((cc - rr * cpr) << 4));
         }
     }
+    cluster_wait();            // rank 0's miss and copy lists are complete
     cluster_arrive_relaxed();  // phase 2
-    cluster_wait();            // rank 0's victims are placed
-    for (int g = cw; g * G < m; g += ncw) {
+    cluster_wait();            // rank 0's victims are placed, its final slots in shared memory
+    const int mc = ld_cluster_s32(r_mc);
+    if (np > 0) {
+        // Each row fetched ahead goes to its entry's final slot: a victim for
+        // a miss, its first occurrence's slot for a repeat that aliases it;
+        // -1 (a repeat refused as an error) drops it.
+        long long dst = -1;
+        if (lane < np) {
+            const int o = ld_cluster_s32(r_out + 4u * (unsigned)((jr % E) * NT + jr / E));
+            if (o >= 0 && o < S) dst = (long long)o * a.R;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int cc = u * 32 + lane;
+            const int rr = cc < nch ? cc / cpr : 0;
+            const long long dg = __shfl_sync(FULL, dst, rr);
+            if (cc < nch && dg >= 0) st_v4(buf_b + dg + ((cc - rr * cpr) << 4), pre[u]);
+        }
+    }
+    // This CTA's share of the copy list.  The next group's entries are read
+    // from rank 0 while the current group's rows are copied.
+    int g = (rank - 1) * NW + warp;
+    int inext = (lane < G && g * G + lane < mc) ? ld_cluster_u16(r_clist + 2u * (unsigned)(g * G + lane)) : -1;
+    for (; g * G < mc; g += ncw) {
         const int r0 = g * G;
         long long src = 0, dst = 0;
-        if (lane < G && r0 + lane < m) {
-            src = (long long)ld_cluster_s32(r_mtok + 4u * (r0 + lane)) * a.R;
-            dst = (long long)ld_cluster_u16(r_vic + 2u * (r0 + lane)) * a.R;
+        if (inext >= 0) {
+            src = (long long)ld_cluster_s32(r_mtok + 4u * (unsigned)inext) * a.R;
+            dst = (long long)ld_cluster_u16(r_vic + 2u * (unsigned)inext) * a.R;
         }
-        const int nrows = (m - r0) < G ? (m - r0) : G;
-        if (early && g == cw) {
-            const int nch = nrows * cpr;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int cc = u * 32 + lane;
-                const int rr = cc < nch ? cc / cpr : 0;
-                const long long dg = __shfl_sync(FULL, dst, rr) + ((cc - rr * cpr) << 4);
-                if (cc < nch) st_v4(buf_b + dg, pre[u]);
-            }
-        } else {
-            copy_row_group<U>(pool_b, buf_b, src, dst, nrows, cpr, lane);
-        }
+        const int gn = g + ncw;
+        inext = (lane < G && gn * G + lane < mc) ? ld_cluster_u16(r_clist + 2u * (unsigned)(gn * G + lane)) : -1;
+        copy_row_group<U>(pool_b, buf_b, src, dst, (mc - r0) < G ? (mc - r0) : G, cpr, lane);
     }
     cluster_arrive_release();  // phase 3: done with rank 0's lists
     cluster_wait();

@@ -360,11 +360,10 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
  *                    their first rows while it chooses the victims, and the
  *                    cluster copies the rows together (more SMs per request
  *                    than FUSED, one launch unlike SPLIT);
- *   HS_COPY_AUTO     (default) cluster when B <= HS_CLUSTER_MAX_BATCH and a
- *                    cluster size of 2 or more fits (hs_cluster_size), else
- *                    fused.  Without such a cluster size: fused when
- *                    B >= HS_FUSED_MIN_BATCH, or when one request's hot
- *                    buffer (S * row_bytes) is at most
+ *   HS_COPY_AUTO     (default) cluster when the device runs a cluster size
+ *                    of 2 or more for the handle (hs_cluster_size).  Without
+ *                    one: fused when B >= HS_FUSED_MIN_BATCH, or when one
+ *                    request's hot buffer (S * row_bytes) is at most
  *                    HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
  *                    much to copy; split otherwise.  A function of the handle
  *                    alone, so hs_resolve_launches answers per handle.
@@ -379,7 +378,7 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
 #define HS_FUSED_MIN_BATCH 16
 #define HS_FUSED_MAX_REQUEST_BYTES (1 << 20)
 #define HS_MAX_CLUSTER   16
-#define HS_CLUSTER_MAX_BATCH 16
+#define HS_CLUSTER_WIDE_BATCH 4
 int hs_set_copy_mode(hs_handle* h, int mode);
 
 /*
@@ -418,10 +417,11 @@ int hs_set_policy(hs_handle* h, int policy);
 int hs_set_tail_mode(hs_handle* h, int mode);
 
 /*
- * CTAs per request in HS_COPY_CLUSTER mode.  n = 0 (the default) picks the
- * largest of 16, 8, 4, 2 for which all B clusters run at once on the device
- * with B * n no larger than its SM count; otherwise 2 <= n <= HS_MAX_CLUSTER,
- * refused (HS_ERR_LIMIT) when the device cannot run clusters of n such CTAs.
+ * CTAs per request in HS_COPY_CLUSTER mode.  n = 0 (the default) picks 16
+ * for up to HS_CLUSTER_WIDE_BATCH requests when all of their clusters run at
+ * once (else 8 under the same condition), and 4 otherwise (2, then 1, when
+ * the device cannot run it); otherwise 2 <= n <= HS_MAX_CLUSTER, refused
+ * (HS_ERR_LIMIT) when the device cannot run clusters of n such CTAs.
  * hs_cluster_size returns the size in use (1 when no cluster size fits: the
  * cluster mode then launches the fused kernel).
  * Source: no passage (a launch-shape knob of this library).

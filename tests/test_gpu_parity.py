@@ -700,11 +700,12 @@ def test_graph_replay_matches_oracle(mode):
 @pytest.mark.parametrize("name,mode", [("tiny_b1_c8k", 1), ("b32_c32k_s4096", 2),
                                        ("b64_c64k_s4096", 2), ("ragged", 1),
                                        ("max_sizes", 1), ("single_slot", 1),
-                                       ("tiny_b1_c8k", 3), ("b32_c32k_s4096", 3),
-                                       ("b64_c64k_s4096", 3), ("b64_c64k_s2048", 3),
-                                       ("b256_c32k_grow_tail512", 3)])
+                                       ("tiny_b1_c8k", 2), ("b32_c32k_s4096", 1),
+                                       ("b64_c64k_s4096", 1), ("b64_c64k_s2048", 1),
+                                       ("b256_c32k_grow_tail512", 1)])
 def test_parity_other_launch_mode(name, mode):
-    """The launch mode that the default (fused from 16 requests up) does not pick."""
+    """The launch modes the default (a cluster of CTAs per request) does not
+    pick: one CTA per request (fused) and the resolve + copy pair (split)."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
     _run_and_compare(wl, copy_mode=mode)
 
@@ -1055,15 +1056,15 @@ def test_device_errors_leave_context_usable():
 
 
 def test_cluster_size_settings():
-    """hs_set_cluster_size: 0 picks the default, 2..HS_MAX_CLUSTER are taken
-    when the device runs them, other values are refused; cluster mode is one
-    launch per step."""
+    """hs_set_cluster_size: 0 picks the default (16 or 8 CTAs up to 4
+    requests, 4 beyond), 2..HS_MAX_CLUSTER are taken when the device runs
+    them, other values are refused; cluster mode is one launch per step."""
     from hierarchical_kv_cache_hs_gb300 import hs
     h = hs.Handle(4, 8192, 1152, 1024, 8)
     try:
         auto = hs.hs_cluster_size(h.h)
-        assert auto in (1, 2, 4, 8, 16)
-        assert auto >= 2  # 4 requests leave most SMs idle
+        assert auto in (8, 16)  # up to 4 requests: wide clusters
+        assert hs.hs_launch_mode(h.h) == hs.HS_COPY_CLUSTER  # the default takes them
         with pytest.raises(hs.HsError):
             hs.hs_set_cluster_size(h.h, 1)
         with pytest.raises(hs.HsError):
@@ -1081,6 +1082,6 @@ def test_cluster_size_settings():
         h.close()
     big = hs.Handle(200, 4096, 64, 256, 16)
     try:
-        assert hs.hs_cluster_size(big.h) == 1  # 200 requests fill the SMs already
+        assert hs.hs_cluster_size(big.h) == 4  # more requests than SMs: clusters of 4
     finally:
         big.close()

@@ -30,8 +30,8 @@ int main()
         if (A % 4 != 0) { printf("K=%d: region A of %d ints misaligns the stamp row\n", K, A); return 1; }
         if (A < (2 << bits)) { printf("K=%d: region A smaller than the hash\n", K); return 1; }
         const int E = (K + HS_RESOLVE_THREADS - 1) / HS_RESOLVE_THREADS;
-        if (A < HS_AGE_SUBHIST * HS_AGE_BINS + E * HS_RESOLVE_THREADS) {
-            printf("K=%d: region A smaller than histograms + out values\n", K);
+        if (2 * A < 2 * (HS_AGE_SUBHIST * HS_AGE_BINS + E * HS_RESOLVE_THREADS) + K) {
+            printf("K=%d: region A smaller than histograms + out values + copy list\n", K);
             return 1;
         }
         const int Ss[] = {K, K + 1, K + 2, K + 3, HS_MAX_SLOTS};
