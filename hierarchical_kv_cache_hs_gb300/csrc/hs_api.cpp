@@ -124,16 +124,18 @@ bool valid(const hs_handle* h)
 
 // The launch of a step: HS_COPY_FUSED, HS_COPY_SPLIT or HS_COPY_CLUSTER.  A
 // cluster mode whose cluster size is 1 runs the fused kernel.  HS_COPY_AUTO:
-// a cluster per request whenever a cluster size of 2 or more runs on the
-// device; otherwise fused, or split below HS_FUSED_MIN_BATCH requests when
-// one request's hot buffer (which bounds what a step gives one CTA to copy)
-// is over HS_FUSED_MAX_REQUEST_BYTES.
+// a cluster per request up to HS_CLUSTER_MAX_BATCH requests when a cluster
+// size of 2 or more runs on the device (beyond it, one CTA per request
+// already fills several waves of the SMs, whose later waves resolve while the
+// earlier ones copy); otherwise fused, or split below HS_FUSED_MIN_BATCH
+// requests when one request's hot buffer (which bounds what a step gives one
+// CTA to copy) is over HS_FUSED_MAX_REQUEST_BYTES.
 int launch_kind(const hs_handle* h)
 {
     if (h->copy_mode == HS_COPY_CLUSTER)
         return h->cluster_n >= 2 ? HS_COPY_CLUSTER : HS_COPY_FUSED;
     if (h->copy_mode != HS_COPY_AUTO) return h->copy_mode;
-    if (h->cluster_n >= 2) return HS_COPY_CLUSTER;
+    if (h->B <= HS_CLUSTER_MAX_BATCH && h->cluster_n >= 2) return HS_COPY_CLUSTER;
     return (h->B >= HS_FUSED_MIN_BATCH ||
             (long long)h->S * h->R <= (long long)HS_FUSED_MAX_REQUEST_BYTES)
                ? HS_COPY_FUSED

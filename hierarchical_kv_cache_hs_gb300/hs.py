@@ -44,6 +44,7 @@ HS_COPY_SPLIT = 2
 HS_COPY_CLUSTER = 3
 HS_MAX_CLUSTER = 16
 HS_CLUSTER_WIDE_BATCH = 4
+HS_CLUSTER_MAX_BATCH = 128
 HS_FUSED_MIN_BATCH = 16
 HS_FUSED_MAX_REQUEST_BYTES = 1 << 20
 

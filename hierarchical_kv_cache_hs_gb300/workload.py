@@ -76,6 +76,9 @@ class GpuWorkload:
         else:
             self.out = torch.full((wl.layers, B, K), -7, dtype=torch.int32, device=self.device)
         self.requests = reqs
+        # The uploads and fills above ran on the current stream; steps may be
+        # launched on any other, so they must be complete first.
+        torch.cuda.synchronize(self.device)
 
     def _fill_pool(self, h, layer, reqs, threads):
         wl = self.wl

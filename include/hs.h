@@ -360,9 +360,11 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
  *                    their first rows while it chooses the victims, and the
  *                    cluster copies the rows together (more SMs per request
  *                    than FUSED, one launch unlike SPLIT);
- *   HS_COPY_AUTO     (default) cluster when the device runs a cluster size
- *                    of 2 or more for the handle (hs_cluster_size).  Without
- *                    one: fused when B >= HS_FUSED_MIN_BATCH, or when one
+ *   HS_COPY_AUTO     (default) cluster when B <= HS_CLUSTER_MAX_BATCH and the
+ *                    device runs a cluster size of 2 or more for the handle
+ *                    (hs_cluster_size); beyond HS_CLUSTER_MAX_BATCH requests
+ *                    fused.  Without such a cluster size: fused when
+ *                    B >= HS_FUSED_MIN_BATCH, or when one
  *                    request's hot buffer (S * row_bytes) is at most
  *                    HS_FUSED_MAX_REQUEST_BYTES, so that no step gives one CTA
  *                    much to copy; split otherwise.  A function of the handle
@@ -379,6 +381,7 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
 #define HS_FUSED_MAX_REQUEST_BYTES (1 << 20)
 #define HS_MAX_CLUSTER   16
 #define HS_CLUSTER_WIDE_BATCH 4
+#define HS_CLUSTER_MAX_BATCH 128
 int hs_set_copy_mode(hs_handle* h, int mode);
 
 /*

@@ -53,6 +53,9 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
     res = GpuResult()
     res.misses = np.zeros((wl.layers, steps, wl.B), dtype=np.int32)
     stream = torch.cuda.Stream()
+    # inputs set up above (a replaced trace, the policies) are on the current
+    # stream: the steps' stream starts after them
+    stream.wait_stream(torch.cuda.current_stream())
     lstreams = [torch.cuda.Stream() for _ in range(wl.layers)] if layer_streams else None
     if graph:
         # Warm the kernels up outside the capture, then restart from the empty state.

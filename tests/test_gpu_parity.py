@@ -702,10 +702,12 @@ def test_graph_replay_matches_oracle(mode):
                                        ("max_sizes", 1), ("single_slot", 1),
                                        ("tiny_b1_c8k", 2), ("b32_c32k_s4096", 1),
                                        ("b64_c64k_s4096", 1), ("b64_c64k_s2048", 1),
-                                       ("b256_c32k_grow_tail512", 1)])
+                                       ("b256_c32k_grow_tail512", 3)])
 def test_parity_other_launch_mode(name, mode):
-    """The launch modes the default (a cluster of CTAs per request) does not
-    pick: one CTA per request (fused) and the resolve + copy pair (split)."""
+    """The launch modes the default does not pick for a workload: one CTA per
+    request (fused) and the resolve + copy pair (split) up to 128 requests,
+    where the default is a cluster per request, and a cluster per request at
+    256 requests, where the default is fused."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
     _run_and_compare(wl, copy_mode=mode)
 
@@ -1082,6 +1084,10 @@ def test_cluster_size_settings():
         h.close()
     big = hs.Handle(200, 4096, 64, 256, 16)
     try:
-        assert hs.hs_cluster_size(big.h) == 4  # more requests than SMs: clusters of 4
+        assert hs.hs_cluster_size(big.h) == 4  # the size cluster mode would take
+        # beyond HS_CLUSTER_MAX_BATCH requests the default takes one CTA per request
+        assert hs.hs_launch_mode(big.h) == hs.HS_COPY_FUSED
+        hs.hs_set_copy_mode(big.h, hs.HS_COPY_CLUSTER)
+        assert hs.hs_launch_mode(big.h) == hs.HS_COPY_CLUSTER
     finally:
         big.close()
