@@ -3,8 +3,8 @@
 // victim selection, and the page-table update with the host -> device row
 // fetch.
 //
-// One CTA of 512 threads per request.  Everything the request's step needs
-// stays in shared memory:
+// One CTA of 512 threads resolves each request.  Everything the request's
+// step needs stays in its shared memory:
 //   - the request's S stamps and S slot -> token entries, loaded once,
 //     together with the top-k row, at the start;
 //   - a 2K-entry open-addressing hash of the row's indices that finds
@@ -28,7 +28,16 @@
 // step carry the current step -- younger than every other slot -- so they
 // are never chosen.
 //
-// Two variants:
+// Three variants:
+//   CLUSTER (hs_swapin_cluster_kernel) a thread-block cluster of 2-16 CTAs
+//           per request.  Rank 0 runs the resolve below; the other ranks
+//           (cluster_helper) gather the page table themselves and load their
+//           share of the candidate misses before rank 0's miss list exists,
+//           then copy rows from rank 0's lists through distributed shared
+//           memory.  Rank 0 ranks the candidates the same way, so every miss
+//           is fetched ahead once or put on its copy list.  The CTAs hand off
+//           through three phases of the hardware cluster barrier.  One
+//           launch; more SMs per request than FUSED.
 //   FUSED   the CTA then updates the tables and copies its own missing rows
 //           from the mapped host pool into the buffer (zero-copy 128-bit
 //           loads, U in flight per lane); the last CTA to finish advances the
@@ -42,9 +51,10 @@
 //   !FUSED  the CTA writes the miss / victim lists to global memory for the
 //           grid-wide copy kernel (hs_copy.cu), which advances the counter.
 //
-// hs_resolve_kernel runs one handle's B CTAs; hs_resolve_layers_kernel runs
-// the same per-CTA body for several independent handles (layers) in one
-// grid, CTA x serving request x mod B of layer x / B.
+// hs_resolve_kernel runs one handle's B CTAs (B clusters for
+// hs_swapin_cluster_kernel); hs_resolve_layers_kernel runs the FUSED per-CTA
+// body for several independent handles (layers) in one grid, CTA x serving
+// request x mod B of layer x / B.
 #include <climits>
 
 #include "hs_internal.h"
