@@ -292,6 +292,8 @@ def run_ours(args, rank, world, dist):
     wl = tg.WORKLOADS[args.workload]
     mode = {"auto": hs.HS_COPY_AUTO, "fused": hs.HS_COPY_FUSED, "split": hs.HS_COPY_SPLIT,
             "cluster": hs.HS_COPY_CLUSTER}[args.copy_mode]
+    hs.hs_set_host_pool_pages({"auto": hs.HS_POOL_PAGES_AUTO, "base": hs.HS_POOL_PAGES_BASE,
+                               "huge": hs.HS_POOL_PAGES_HUGE}[args.pool_pages])
     total_steps = PRIME_STEPS + args.warmup + args.steps
     # Several layers: one launch for all of them, or one call per layer.
     one = args.layer_launch == "one" and wl.layers > 1
@@ -319,7 +321,10 @@ def run_ours(args, rank, world, dist):
         # cluster of CTAs per request) or two (split).
         kind = hs.hs_launch_mode(w.handles[0].h)
         res = {"fused": kind != hs.HS_COPY_SPLIT, "cluster": kind == hs.HS_COPY_CLUSTER,
-               "cluster_size": hs.hs_cluster_size(w.handles[0].h)}
+               "cluster_size": hs.hs_cluster_size(w.handles[0].h),
+               "pool_pages": ("huge-page memory, cudaHostRegister"
+                              if hs.hs_host_pool_pages(w.handles[0].h) == hs.HS_POOL_PAGES_HUGE
+                              else "cudaHostAlloc")}
         try:
             def stats_sum(key):
                 return sum(hs.hs_stats(h.h)[key] for h in w.handles)
@@ -559,6 +564,7 @@ def run_ours(args, rank, world, dist):
             "launch_mode": ("fused, all layers in one launch" if one else
                             "cluster of %d CTAs per request" % res["cluster_size"] if cl else
                             "fused" if fused else "split"),
+            "host_pool": res["pool_pages"],
             "misses_per_step_mean": statistics.mean(res["misses_per_step"]),
             "inplace_per_step_mean": res["inplace"] / args.steps,
             "e2e": {"value": e2e_value, "unit": "resolves/s",
@@ -817,6 +823,8 @@ def main():
                          "stream and on one stream per layer")
     ap.add_argument("--copy-mode", choices=["auto", "fused", "split", "cluster"], default="auto",
                     help="launch mode of the step (identical results; see hs_set_copy_mode)")
+    ap.add_argument("--pool-pages", choices=["auto", "base", "huge"], default="auto",
+                    help="host pool placement (identical results; see hs_set_host_pool_pages)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -2,7 +2,11 @@
 // argument checks, launches and state export.  The host never reads device
 // data on the resolve path; everything it enqueues is graph-capturable.
 #include <cuda_runtime.h>
+#include <sys/mman.h>
+#include <unistd.h>
 
+#include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <functional>
@@ -22,6 +26,8 @@ struct hs_handle {
     uint8_t* d_buf;        // [B][S+T][R]
     uint8_t* h_pool;       // pinned, mapped [B][H][R]
     uint8_t* d_pool;       // device address of h_pool
+    size_t pool_map_len;   // > 0: h_pool is an mmap of this length, registered
+                           // with CUDA; 0: from cudaHostAlloc
     int32_t* d_miss_tok;   // [B][S] scratch: this step's miss tokens
     int32_t* d_miss_slot;  // [B][S] scratch: their victim slots
     int32_t* d_miss_cnt;   // [B]
@@ -72,6 +78,77 @@ cudaError_t dalloc(T** p, size_t n)
     return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
 }
 
+// How host pools are placed (hs_set_host_pool_pages), process-wide.
+std::atomic<int> g_pool_pages{HS_POOL_PAGES_AUTO};
+
+// Size of a transparent huge page on this host (the kernel's PMD mapping
+// size), or 0 when the kernel offers none.
+size_t huge_page_bytes()
+{
+    static const size_t bytes = [] {
+        size_t v = 0;
+        if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+            unsigned long long x = 0;
+            if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+            std::fclose(f);
+        }
+        return v;
+    }();
+    return bytes;
+}
+
+// The host pool, n bytes.  A pool of at least one huge page (or any size under
+// HS_POOL_PAGES_HUGE) is placed in anonymous memory aligned to the huge-page
+// size and advised for huge pages before its first touch, then page-locked and
+// mapped with cudaHostRegister, so the GPU can map it with large pages: with
+// the base pages of cudaHostAlloc, a pool of tens of GB read from many SMs at
+// once spends much of the step on address translation.  Whether the kernel
+// backs the range with huge pages is up to it (memory fragmentation); any
+// failure here falls back to cudaHostAlloc.
+bool alloc_pool(hs_handle* h, size_t n)
+{
+    const int mode = g_pool_pages.load();
+    const size_t hp = huge_page_bytes();
+    const long pg = sysconf(_SC_PAGESIZE);
+    if (mode != HS_POOL_PAGES_BASE && hp > 0 && pg > 0 &&
+        (n >= hp || (mode == HS_POOL_PAGES_HUGE && n > 0))) {
+        const size_t len = (n + (size_t)pg - 1) / (size_t)pg * (size_t)pg;
+        void* m = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+        if (m != MAP_FAILED) {
+            const uintptr_t lo = (uintptr_t)m, hi = lo + len + hp;
+            const uintptr_t a = (lo + hp - 1) / hp * hp;  // a multiple of the page size too
+            if (a > lo) munmap(m, a - lo);
+            if (hi > a + len) munmap(reinterpret_cast<void*>(a + len), hi - (a + len));
+            void* p = reinterpret_cast<void*>(a);
+            madvise(p, len, MADV_HUGEPAGE);
+            if (cudaHostRegister(p, n, cudaHostRegisterMapped) == cudaSuccess) {
+                h->h_pool = static_cast<uint8_t*>(p);
+                h->pool_map_len = len;
+                return true;
+            }
+            cudaGetLastError();
+            munmap(p, len);
+        }
+    }
+    void* p = nullptr;
+    if (cudaHostAlloc(&p, n ? n : 1, cudaHostAllocMapped) != cudaSuccess) return false;
+    h->h_pool = static_cast<uint8_t*>(p);
+    h->pool_map_len = 0;
+    return true;
+}
+
+void free_pool(hs_handle* h)
+{
+    if (!h->h_pool) return;
+    if (h->pool_map_len > 0) {
+        cudaHostUnregister(h->h_pool);
+        munmap(h->h_pool, h->pool_map_len);
+    } else {
+        cudaFreeHost(h->h_pool);
+    }
+    h->h_pool = nullptr;
+}
+
 void free_all(hs_handle* h)
 {
     if (!h) return;
@@ -87,7 +164,7 @@ void free_all(hs_handle* h)
     cudaFree(h->d_done);
     cudaFree(h->d_stage_in);
     cudaFree(h->d_stage_out);
-    if (h->h_pool) cudaFreeHost(h->h_pool);
+    free_pool(h);
     if (h->ce_h_stage) cudaFreeHost(h->ce_h_stage);
     cudaFree(h->ce_d_stage);
     if (h->ce_h_cnt) cudaFreeHost(h->ce_h_cnt);
@@ -222,12 +299,10 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
               dalloc(&h->d_stage_in, B * kmax) == cudaSuccess &&
               dalloc(&h->d_stage_out, B * kmax) == cudaSuccess;
     if (ok) {
-        void* p = nullptr;
-        ok = cudaHostAlloc(&p, h->pool_bytes ? h->pool_bytes : 1, cudaHostAllocMapped) == cudaSuccess;
+        ok = alloc_pool(h, h->pool_bytes);
         if (ok) {
-            h->h_pool = static_cast<uint8_t*>(p);
             void* dp = nullptr;
-            ok = cudaHostGetDevicePointer(&dp, p, 0) == cudaSuccess;
+            ok = cudaHostGetDevicePointer(&dp, h->h_pool, 0) == cudaSuccess;
             h->d_pool = static_cast<uint8_t*>(dp);
         }
     }
@@ -704,6 +779,22 @@ int hs_stats(hs_handle* h, hs_stats_t* out, int32_t* last_miss)
 
 uint8_t* hs_host_pool(hs_handle* h) { return valid(h) ? h->h_pool : nullptr; }
 size_t hs_host_pool_bytes(hs_handle* h) { return valid(h) ? h->pool_bytes : 0; }
+
+int hs_set_host_pool_pages(int mode)
+{
+    if (mode != HS_POOL_PAGES_AUTO && mode != HS_POOL_PAGES_BASE && mode != HS_POOL_PAGES_HUGE)
+        return HS_ERR_ARG;
+    g_pool_pages.store(mode);
+    return HS_OK;
+}
+
+int hs_host_pool_pages(hs_handle* h)
+{
+    if (!valid(h)) return HS_ERR_ARG;
+    return h->pool_map_len > 0 ? HS_POOL_PAGES_HUGE : HS_POOL_PAGES_BASE;
+}
+
+size_t hs_huge_page_bytes(void) { return huge_page_bytes(); }
 uint8_t* hs_device_buffer(hs_handle* h) { return valid(h) ? h->d_buf : nullptr; }
 size_t hs_device_buffer_bytes(hs_handle* h) { return valid(h) ? h->buf_bytes : 0; }
 

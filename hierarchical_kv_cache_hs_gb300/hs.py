@@ -45,6 +45,9 @@ HS_COPY_CLUSTER = 3
 HS_MAX_CLUSTER = 16
 HS_CLUSTER_WIDE_BATCH = 4
 HS_CLUSTER_MAX_BATCH = 128
+HS_POOL_PAGES_AUTO = 0
+HS_POOL_PAGES_BASE = 1
+HS_POOL_PAGES_HUGE = 2
 HS_FUSED_MIN_BATCH = 16
 HS_FUSED_MAX_REQUEST_BYTES = 1 << 20
 
@@ -91,6 +94,9 @@ def _load():
         "hs_stats": ([P, ctypes.POINTER(hs_stats_t), P], I),
         "hs_host_pool": ([P], P),
         "hs_host_pool_bytes": ([P], Z),
+        "hs_set_host_pool_pages": ([I], I),
+        "hs_host_pool_pages": ([P], I),
+        "hs_huge_page_bytes": ([], Z),
         "hs_device_buffer": ([P], P),
         "hs_device_buffer_bytes": ([P], Z),
         "hs_set_lengths": ([P, P], I),
@@ -244,6 +250,22 @@ def hs_host_pool(h: int) -> int:
 
 def hs_host_pool_bytes(h: int) -> int:
     return int(lib.hs_host_pool_bytes(h))
+
+
+def hs_set_host_pool_pages(mode: int) -> None:
+    """Placement of the host pools of handles created from now on (HS_POOL_PAGES_*)."""
+    _check(lib.hs_set_host_pool_pages(int(mode)), "hs_set_host_pool_pages")
+
+
+def hs_host_pool_pages(h: int) -> int:
+    r = lib.hs_host_pool_pages(h)
+    if r < 0:
+        raise HsError(r, "hs_host_pool_pages")
+    return int(r)
+
+
+def hs_huge_page_bytes() -> int:
+    return int(lib.hs_huge_page_bytes())
 
 
 def hs_device_buffer(h: int) -> int:

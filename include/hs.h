@@ -119,7 +119,8 @@ typedef struct {
  *   resident_tail  T >= 0, device-resident tail tokens (0 = no mixed residency)
  * All tables start empty, stamps 0, step 0, every request's length = C
  * (use hs_set_lengths for a growing context).  The host pool is allocated
- * but not filled: write the cold rows through hs_host_pool before resolving.
+ * but not filled: write the cold rows through hs_host_pool before resolving
+ * (its placement follows hs_set_host_pool_pages).
  * Returns HS_OK and *out, or an HS_ERR_* code (then *out = NULL).
  * Source: HiSparse blog, "ベンチマークテスト" (the deployment's top_k,
  * device_buffer_size and host_to_device_ratio); vLLM Hybrid HiSparse post,
@@ -247,6 +248,37 @@ int hs_stats(hs_handle* h, hs_stats_t* out, int32_t* last_miss);
  * host memory); vLLM Hybrid HiSparse post, "Mixed Residency" (pinned host memory). */
 uint8_t* hs_host_pool(hs_handle* h);
 size_t hs_host_pool_bytes(hs_handle* h);
+
+/*
+ * Where hs_create places host pools, for the whole process (later handles
+ * only; a handle keeps the pool it was created with):
+ *   HS_POOL_PAGES_AUTO  (default) a pool of at least one transparent huge page
+ *                       (hs_huge_page_bytes) goes into anonymous memory aligned
+ *                       to that size and advised for huge pages, then is
+ *                       page-locked and mapped with cudaHostRegister; smaller
+ *                       pools come from cudaHostAlloc(..., cudaHostAllocMapped)
+ *   HS_POOL_PAGES_BASE  always cudaHostAlloc
+ *   HS_POOL_PAGES_HUGE  the huge-page placement for any non-empty pool, when
+ *                       the host has huge pages
+ * The huge-page placement falls back to cudaHostAlloc when mmap or the
+ * registration fails; whether the kernel backs the range with huge pages
+ * depends on its free memory.  Why it matters: with base pages, a pool of tens
+ * of GB whose rows are read by several SMs per request (cluster and split
+ * launches) spends much of a step on address translation; huge pages let the
+ * GPU map it with large pages.  Either placement is pinned, mapped and read
+ * the same way, with bit-identical results.  Returns HS_OK or HS_ERR_ARG
+ * (unknown mode).  hs_host_pool_pages reports a handle's placement
+ * (HS_POOL_PAGES_HUGE or HS_POOL_PAGES_BASE); hs_huge_page_bytes is the host's
+ * transparent huge page size (0: none).
+ * Source: no passage (host memory placement; the pages keep cold KV in
+ * pinned host memory without saying how it is mapped).
+ */
+#define HS_POOL_PAGES_AUTO 0
+#define HS_POOL_PAGES_BASE 1
+#define HS_POOL_PAGES_HUGE 2
+int hs_set_host_pool_pages(int mode);
+int hs_host_pool_pages(hs_handle* h);
+size_t hs_huge_page_bytes(void);
 
 /* Device pointer of the buffer [B][S+T][R] that out_slot indexes; its size in bytes.
  * Source: HiSparse blog, "HiSparseの設計" (the hot device buffer in HBM);
@@ -468,9 +500,10 @@ int hs_profile_events(hs_handle* h, void* before_copy, void* after_copy);
  *   tok_slot [B][C], slot_tok [B][S] (start at -1), stamp [B][S] (start at 0),
  *   lengths [B], device_buffer [B][S+T][R]: device memory.
  *   host_pool [B][host_rows][R]: pinned host memory mapped into the device
- *   address space (cudaHostAlloc with cudaHostAllocMapped), host pointer;
- *   all B * host_rows * R bytes must lie in the allocation that holds its
- *   first byte, as the driver reports it.
+ *   address space (cudaHostAlloc with cudaHostAllocMapped, cudaHostRegister
+ *   with cudaHostRegisterMapped, or a handle's hs_host_pool), host pointer;
+ *   all B * host_rows * R bytes must lie in the allocation or registration
+ *   that holds its first byte, as the driver reports it.
  *   control: device memory, one hs_control_t, zeroed by the caller before
  *   the first step; the step counter and counters advance in it.
  * Alignment: host_pool and device_buffer 16 bytes, control 8 bytes, the

@@ -712,6 +712,42 @@ def test_parity_other_launch_mode(name, mode):
     _run_and_compare(wl, copy_mode=mode)
 
 
+@pytest.mark.parametrize("placement", ["base", "huge"])
+@pytest.mark.parametrize("name,mode", [("ragged", 3), ("odd_k", 2), ("b32_c32k_s4096", 1),
+                                       ("b32_c32k_s4096", 3)])
+def test_parity_host_pool_placement(placement, name, mode):
+    """Both host-pool placements give the oracle's results: cudaHostAlloc, and
+    anonymous memory advised for huge pages and registered with
+    cudaHostRegister (forced here for pools of any size).  With the default
+    placement, pools of at least one huge page take the second."""
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    want = hs.HS_POOL_PAGES_BASE if placement == "base" else hs.HS_POOL_PAGES_HUGE
+    if want == hs.HS_POOL_PAGES_HUGE and hs.hs_huge_page_bytes() == 0:
+        pytest.skip("the host offers no transparent huge pages")
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    seen = []
+    hs.hs_set_host_pool_pages(want)
+    try:
+        res = gpu_run(wl, copy_mode=mode, setup=lambda w: seen.extend(
+            hs.hs_host_pool_pages(h.h) for h in w.handles))
+    finally:
+        hs.hs_set_host_pool_pages(hs.HS_POOL_PAGES_AUTO)
+    try:
+        assert seen == [want] * wl.layers
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+    finally:
+        res.workload.close()
+    # the default placement follows the pool's size
+    h = hs.Handle(1, 64, 16, 8, 8, 0)
+    try:
+        big = hs.hs_host_pool_bytes(h.h) >= hs.hs_huge_page_bytes() > 0
+        assert hs.hs_host_pool_pages(h.h) == (hs.HS_POOL_PAGES_HUGE if big else hs.HS_POOL_PAGES_BASE)
+    finally:
+        h.close()
+
+
 @pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 2),
                                        ("tiny_b1_c8k", 0), ("b256_c32k_grow_tail512", 0),
                                        ("ragged", 1), ("odd_k", 1), ("odd_k", 2),

@@ -108,16 +108,27 @@ def _state(B, C, S, T, R, dev="cuda"):
                 control=torch.zeros(8, dtype=torch.int32, device=dev))
 
 
-def test_noalloc_refuses_misaligned_pointers_and_short_pools():
+@pytest.mark.parametrize("placement", ["base", "huge"])
+def test_noalloc_refuses_misaligned_pointers_and_short_pools(placement):
     """Host-side checks before anything is enqueued: a pool that the driver
     reports shorter than B * host_rows * R bytes, and pointers that break the
     kernels' alignment, return HS_ERR_ARG and leave the caller's state as it
-    was; a correct call afterwards still runs."""
+    was; a correct call afterwards still runs.  The pool is a handle's, in
+    either placement: cudaHostAlloc, or a cudaHostRegister registration of
+    exactly the pool's bytes."""
     from hierarchical_kv_cache_hs_gb300 import hs
+    want = hs.HS_POOL_PAGES_BASE if placement == "base" else hs.HS_POOL_PAGES_HUGE
+    if want == hs.HS_POOL_PAGES_HUGE and hs.hs_huge_page_bytes() == 0:
+        pytest.skip("the host offers no transparent huge pages")
     # a 4 MiB pool (2 requests x 2048 rows x 1 KiB), a whole number of pages
     B, C, S, K, R, ratio = 2, 1024, 128, 64, 1024, 16
-    h = hs.Handle(B, C, R, S, ratio, 0)  # only for its pinned host pool
+    hs.hs_set_host_pool_pages(want)
     try:
+        h = hs.Handle(B, C, R, S, ratio, 0)  # only for its pinned host pool
+    finally:
+        hs.hs_set_host_pool_pages(hs.HS_POOL_PAGES_AUTO)
+    try:
+        assert hs.hs_host_pool_pages(h.h) == want
         st = _state(B, C, S, 0, R)
         topk = torch.arange(K, dtype=torch.int32, device="cuda").repeat(B, 1).contiguous()
         out = torch.full((B, K), -7, dtype=torch.int32, device="cuda")
