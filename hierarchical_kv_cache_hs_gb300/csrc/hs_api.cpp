@@ -97,21 +97,25 @@ size_t huge_page_bytes()
     return bytes;
 }
 
-// The host pool, n bytes.  A pool of at least one huge page (or any size under
-// HS_POOL_PAGES_HUGE) is placed in anonymous memory aligned to the huge-page
-// size and advised for huge pages before its first touch, then page-locked and
-// mapped with cudaHostRegister, so the GPU can map it with large pages: with
-// the base pages of cudaHostAlloc, a pool of tens of GB read from many SMs at
-// once spends much of the step on address translation.  Whether the kernel
-// backs the range with huge pages is up to it (memory fragmentation); any
-// failure here falls back to cudaHostAlloc.
+// The host pool, n bytes.  A pool of at least HS_POOL_HUGE_MIN_BYTES and one
+// huge page (or any size under HS_POOL_PAGES_HUGE) is placed in anonymous
+// memory aligned to the huge-page size and advised for huge pages before its
+// first touch, then page-locked and mapped with cudaHostRegister, so the GPU
+// can map it with large pages: with the base pages of cudaHostAlloc, a pool of
+// tens of GB read from several SMs per request spends much of the step on
+// address translation.  Smaller pools stay in cudaHostAlloc memory, whose
+// first steps after set-up run at full speed (the huge-page placement's
+// first seconds of steps are slow and uneven).  Whether the kernel backs the
+// range with huge pages is up to it (memory fragmentation); any failure here
+// falls back to cudaHostAlloc.
 bool alloc_pool(hs_handle* h, size_t n)
 {
     const int mode = g_pool_pages.load();
     const size_t hp = huge_page_bytes();
     const long pg = sysconf(_SC_PAGESIZE);
+    const bool big = n >= hp && n >= (size_t)HS_POOL_HUGE_MIN_BYTES;
     if (mode != HS_POOL_PAGES_BASE && hp > 0 && pg > 0 &&
-        (n >= hp || (mode == HS_POOL_PAGES_HUGE && n > 0))) {
+        (big || (mode == HS_POOL_PAGES_HUGE && n > 0))) {
         const size_t len = (n + (size_t)pg - 1) / (size_t)pg * (size_t)pg;
         void* m = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
         if (m != MAP_FAILED) {

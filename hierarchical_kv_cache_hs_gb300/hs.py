@@ -48,6 +48,7 @@ HS_CLUSTER_MAX_BATCH = 128
 HS_POOL_PAGES_AUTO = 0
 HS_POOL_PAGES_BASE = 1
 HS_POOL_PAGES_HUGE = 2
+HS_POOL_HUGE_MIN_BYTES = 1 << 34
 HS_FUSED_MIN_BATCH = 16
 HS_FUSED_MAX_REQUEST_BYTES = 1 << 20
 

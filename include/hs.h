@@ -252,11 +252,12 @@ size_t hs_host_pool_bytes(hs_handle* h);
 /*
  * Where hs_create places host pools, for the whole process (later handles
  * only; a handle keeps the pool it was created with):
- *   HS_POOL_PAGES_AUTO  (default) a pool of at least one transparent huge page
- *                       (hs_huge_page_bytes) goes into anonymous memory aligned
- *                       to that size and advised for huge pages, then is
- *                       page-locked and mapped with cudaHostRegister; smaller
- *                       pools come from cudaHostAlloc(..., cudaHostAllocMapped)
+ *   HS_POOL_PAGES_AUTO  (default) a pool of at least HS_POOL_HUGE_MIN_BYTES
+ *                       and one transparent huge page (hs_huge_page_bytes)
+ *                       goes into anonymous memory aligned to that size and
+ *                       advised for huge pages, then is page-locked and mapped
+ *                       with cudaHostRegister; smaller pools come from
+ *                       cudaHostAlloc(..., cudaHostAllocMapped)
  *   HS_POOL_PAGES_BASE  always cudaHostAlloc
  *   HS_POOL_PAGES_HUGE  the huge-page placement for any non-empty pool, when
  *                       the host has huge pages
@@ -265,14 +266,17 @@ size_t hs_host_pool_bytes(hs_handle* h);
  * depends on its free memory.  Why it matters: with base pages, a pool of tens
  * of GB whose rows are read by several SMs per request (cluster and split
  * launches) spends much of a step on address translation; huge pages let the
- * GPU map it with large pages.  Either placement is pinned, mapped and read
- * the same way, with bit-identical results.  Returns HS_OK or HS_ERR_ARG
+ * GPU map it with large pages.  The first seconds of steps on a huge-page pool
+ * are slow and uneven (measured; the cause is not known), hence the size
+ * floor.  Either placement is pinned, mapped and read the same way, with
+ * bit-identical results.  Returns HS_OK or HS_ERR_ARG
  * (unknown mode).  hs_host_pool_pages reports a handle's placement
  * (HS_POOL_PAGES_HUGE or HS_POOL_PAGES_BASE); hs_huge_page_bytes is the host's
  * transparent huge page size (0: none).
  * Source: no passage (host memory placement; the pages keep cold KV in
  * pinned host memory without saying how it is mapped).
  */
+#define HS_POOL_HUGE_MIN_BYTES (1ull << 34) /* 16 GiB */
 #define HS_POOL_PAGES_AUTO 0
 #define HS_POOL_PAGES_BASE 1
 #define HS_POOL_PAGES_HUGE 2

@@ -169,3 +169,16 @@ def test_noalloc_binding_checks_torch_arguments(hs):
             hs.hs_resolve_noalloc(B, C, R, S, H, 0, a["topk_idx"], K, a["out_slot"], a["tok_slot"],
                                   a["slot_tok"], a["stamp"], a["lengths"], a["host_pool"],
                                   a["device_buffer"], a["control"])
+
+
+def test_pool_placement_calls_check_their_arguments(hs):
+    """The placement switch takes the three modes only; a NULL handle has none."""
+    try:
+        for mode in (hs.HS_POOL_PAGES_BASE, hs.HS_POOL_PAGES_HUGE, hs.HS_POOL_PAGES_AUTO):
+            assert hs.lib.hs_set_host_pool_pages(mode) == 0
+        assert hs.lib.hs_set_host_pool_pages(3) == hs.HS_ERR_ARG
+        assert hs.lib.hs_set_host_pool_pages(-1) == hs.HS_ERR_ARG
+    finally:
+        hs.lib.hs_set_host_pool_pages(hs.HS_POOL_PAGES_AUTO)
+    assert hs.lib.hs_host_pool_pages(None) == hs.HS_ERR_ARG
+    assert hs.hs_huge_page_bytes() >= 0

@@ -35,7 +35,7 @@ def header_defines():
         m = re.match(r"#define\s+(HS_\w+)\s+(.+?)\s*(/\*.*)?$", line)
         if not m or m.group(1) == "HS_H":
             continue
-        expr = m.group(2)
+        expr = re.sub(r"\b(\d+)(?:ull|ul|ll|u|l)\b", r"\1", m.group(2), flags=re.I)  # C suffixes
         if not re.fullmatch(r"[\w\s()+*<>x-]+", expr):
             continue
         out[m.group(1)] = _value(ast.parse(expr, mode="eval"), out)
@@ -47,6 +47,7 @@ def test_header_constants_parse():
     # the values every caller depends on
     assert d["HS_OK"] == 0 and d["HS_ERR_ARG"] < 0
     assert d["HS_FUSED_MAX_REQUEST_BYTES"] == 1 << 20
+    assert d["HS_POOL_HUGE_MIN_BYTES"] == 16 << 30
     assert d["HS_NOALLOC_SCRATCH_BYTES"] == 8 * d["HS_NOALLOC_MAX_ENTRIES"] + 4 * d["HS_MAX_BATCH"]
 
 

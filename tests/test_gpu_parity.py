@@ -719,7 +719,7 @@ def test_parity_host_pool_placement(placement, name, mode):
     """Both host-pool placements give the oracle's results: cudaHostAlloc, and
     anonymous memory advised for huge pages and registered with
     cudaHostRegister (forced here for pools of any size).  With the default
-    placement, pools of at least one huge page take the second."""
+    placement, only pools of at least HS_POOL_HUGE_MIN_BYTES take the second."""
     from gpu_harness import check_counters, compare, gpu_run
     from hierarchical_kv_cache_hs_gb300 import hs
     want = hs.HS_POOL_PAGES_BASE if placement == "base" else hs.HS_POOL_PAGES_HUGE
@@ -739,11 +739,11 @@ def test_parity_host_pool_placement(placement, name, mode):
         check_counters(wl, res, tot, err)
     finally:
         res.workload.close()
-    # the default placement follows the pool's size
-    h = hs.Handle(1, 64, 16, 8, 8, 0)
+    # the default placement keeps pools below the size floor in cudaHostAlloc memory
+    h = hs.Handle(wl.B, wl.C, wl.row_bytes, wl.S, wl.host_ratio, wl.T)
     try:
-        big = hs.hs_host_pool_bytes(h.h) >= hs.hs_huge_page_bytes() > 0
-        assert hs.hs_host_pool_pages(h.h) == (hs.HS_POOL_PAGES_HUGE if big else hs.HS_POOL_PAGES_BASE)
+        assert hs.hs_host_pool_bytes(h.h) < hs.HS_POOL_HUGE_MIN_BYTES
+        assert hs.hs_host_pool_pages(h.h) == hs.HS_POOL_PAGES_BASE
     finally:
         h.close()
 
