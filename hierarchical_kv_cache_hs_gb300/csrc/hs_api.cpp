@@ -3,6 +3,7 @@
 // data on the resolve path; everything it enqueues is graph-capturable.
 #include <cuda_runtime.h>
 #include <sys/mman.h>
+#include <sys/syscall.h>
 #include <unistd.h>
 
 #include <atomic>
@@ -97,6 +98,23 @@ size_t huge_page_bytes()
     return bytes;
 }
 
+// Ask for the pages of [p, p + len) on the host NUMA node nearest the GPU,
+// before their first touch, as a preference (MPOL_PREFERRED).  Nothing
+// happens when the device reports no node or the call fails.
+void prefer_gpu_node(void* p, size_t len, int device)
+{
+    int node = -1;
+    if (cudaDeviceGetAttribute(&node, cudaDevAttrHostNumaId, device) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    if (node < 0 || node >= 1024) return;
+    unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {};
+    mask[node / (8 * sizeof(unsigned long))] = 1ul << (node % (8 * sizeof(unsigned long)));
+    const int kPreferred = 1;  // MPOL_PREFERRED
+    syscall(SYS_mbind, p, len, kPreferred, mask, (unsigned long)(node + 2), 0u);
+}
+
 // The host pool, n bytes.  A pool of at least HS_POOL_HUGE_MIN_BYTES and one
 // huge page (or any size under HS_POOL_PAGES_HUGE) is placed in anonymous
 // memory aligned to the huge-page size and advised for huge pages before its
@@ -125,6 +143,10 @@ bool alloc_pool(hs_handle* h, size_t n)
             if (hi > a + len) munmap(reinterpret_cast<void*>(a + len), hi - (a + len));
             void* p = reinterpret_cast<void*>(a);
             madvise(p, len, MADV_HUGEPAGE);
+            // A forked child does not inherit the pool (it would otherwise copy
+            // every pinned page at the fork).
+            madvise(p, len, MADV_DONTFORK);
+            prefer_gpu_node(p, len, h->device);
             if (cudaHostRegister(p, n, cudaHostRegisterMapped) == cudaSuccess) {
                 h->h_pool = static_cast<uint8_t*>(p);
                 h->pool_map_len = len;

@@ -266,7 +266,10 @@ size_t hs_host_pool_bytes(hs_handle* h);
  *   HS_POOL_PAGES_BASE  always cudaHostAlloc
  *   HS_POOL_PAGES_HUGE  the huge-page placement for any non-empty pool, when
  *                       the host has huge pages
- * The huge-page placement falls back to cudaHostAlloc when mmap or the
+ * A huge-page pool prefers the host NUMA node nearest the GPU
+ * (cudaDevAttrHostNumaId, when the device names one) and is not inherited by
+ * forked children (MADV_DONTFORK; a cudaHostAlloc pool is not either).  The
+ * huge-page placement falls back to cudaHostAlloc when mmap or the
  * registration fails; whether the kernel backs the range with huge pages
  * depends on its free memory.  Why it matters: with base pages, a pool of tens
  * of GB whose rows are read by several SMs per request (cluster and split
