@@ -748,6 +748,29 @@ def test_parity_host_pool_placement(placement, name, mode):
         h.close()
 
 
+def test_parity_pool_past_the_huge_page_floor():
+    """A pool of HS_POOL_HUGE_MIN_BYTES or more takes the huge-page placement by
+    default (where the host offers huge pages), and its steps match the oracle:
+    16 requests with a 933,888-token context, 17.2 GB of pool, the default
+    launch (a cluster per request); the first and last requests are compared."""
+    from gpu_harness import compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    S, ratio = 2048, 456
+    wl = tg.Workload("pool_17g", 23, B=16, C=S * ratio, K=1024, S=S, T=0, host_ratio=ratio,
+                     layers=1, steps=6, len0=S * ratio, grow=0, carry_pct=70, zipf_pct=20,
+                     third=tg.THIRD_UNIFORM)
+    assert wl.B * wl.H * wl.row_bytes >= hs.HS_POOL_HUGE_MIN_BYTES
+    seen = []
+    res = gpu_run(wl, setup=lambda w: seen.extend(hs.hs_host_pool_pages(h.h) for h in w.handles))
+    try:
+        want = hs.HS_POOL_PAGES_HUGE if hs.hs_huge_page_bytes() > 0 else hs.HS_POOL_PAGES_BASE
+        assert seen == [want]
+        assert hs.hs_launch_mode(res.workload.handles[0].h) == hs.HS_COPY_CLUSTER
+        compare(wl, res, requests=[0, wl.B - 1])
+    finally:
+        res.workload.close()
+
+
 @pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 2),
                                        ("tiny_b1_c8k", 0), ("b256_c32k_grow_tail512", 0),
                                        ("ragged", 1), ("odd_k", 1), ("odd_k", 2),
