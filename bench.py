@@ -41,6 +41,9 @@ PRIME_STEPS = 10
 # at the time of the capture.  A figure whose fingerprint no longer matches is
 # not reported (the kernel has changed since it was measured).
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+# Buffer sizes of the miss-count curve (top-k 2048, so 2048 is the smallest) and its requests.
+MISS_CURVE_SLOTS = (2048, 2560, 3072, 4096, 6144, 8192)
+MISS_CURVE_REQUESTS = 16
 # The files that define each kernel's code.
 KERNEL_SOURCES = {
     "hs_resolve_kernel_fused": ["hs_resolve.cu", "hs_internal.h"],
@@ -505,10 +508,46 @@ def run_ours(args, rank, world, dist):
             w.close()
         return out
 
+    def miss_curve(base):
+        """Misses per request per step against the buffer size, for both policies: the
+        curve behind the blog's miss-count figure (buffer size x eviction policy), on the
+        first MISS_CURVE_REQUESTS requests of the workload's trace (the generator keys each
+        request's trace by its id, so they are the same requests as in the full run).
+        Counting only; the steps are not timed."""
+        import numpy as np
+        B = min(MISS_CURVE_REQUESTS, base.B)
+        curve = {"requests": B, "steps": args.steps, "buffer_slots": list(MISS_CURVE_SLOTS),
+                 "lru": [], "fifo": []}
+        stream = torch.cuda.Stream(device=dev)
+        for S in MISS_CURVE_SLOTS:
+            wl = base.with_(B=B, S=S, host_ratio=-(-base.cold // S))
+            w = GpuWorkload(wl, steps=total_steps, record=False, copy_mode=mode)
+            try:
+                last = np.zeros(B, dtype=np.int32)
+                for pname, pol in (("lru", hs.HS_POLICY_LRU), ("fifo", hs.HS_POLICY_FIFO)):
+                    w.reset()
+                    for h in w.handles:
+                        hs.hs_set_policy(h.h, pol)
+                    misses = 0
+                    with torch.cuda.stream(stream):
+                        for s in range(PRIME_STEPS + args.warmup):
+                            w.launch_step(s, stream)
+                        for i in range(args.steps):
+                            w.launch_step(PRIME_STEPS + args.warmup + i, stream)
+                            hs.hs_stats(w.handles[0].h, last)
+                            misses += int(last.sum())
+                    curve[pname].append(misses / (B * args.steps))
+            finally:
+                w.close()
+        return curve
+
     sweep = {}
+    curve = None
     if not args.no_sweep and args.workload == "b64_c64k_s4096":
         for name in ("b64_c64k_s4096", "b64_c64k_s2048"):
             sweep[name] = policy_sweep(tg.WORKLOADS[name])
+        if rank == 0:
+            curve = miss_curve(tg.WORKLOADS["b64_c64k_s4096"])
 
     def summarize(wl, res, one):
         """The metric, both rooflines and the end-to-end figure of one measured workload."""
@@ -617,6 +656,8 @@ def run_ours(args, rank, world, dist):
         }
     if sweep:
         line["sweep"] = sweep
+    if curve is not None:
+        line["miss_curve"] = curve
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args, total_steps)
 
