@@ -29,6 +29,7 @@ E_NOROOM = 8
 
 POLICY_LRU = 0
 POLICY_FIFO = 1
+POLICY_RANDOM = 2
 
 
 def build(force: bool = False) -> str:
@@ -69,6 +70,12 @@ def load_library(path: str):
         lib.or_resolve_full.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
                                         i32, i32, i32]
         lib.or_resolve_full.restype = i32
+    if hasattr(lib, "or_resolve_keyed"):
+        lib.or_resolve_keyed.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, i32, P, P,
+                                         i32, i32, i32, i32, ctypes.c_uint64]
+        lib.or_resolve_keyed.restype = i32
+        lib.or_splitmix64_at.argtypes = [ctypes.c_uint64]
+        lib.or_splitmix64_at.restype = ctypes.c_uint64
     lib.or_append.argtypes = [i32, i32, i32, i32, P, P, P]
     lib.or_append.restype = i32
     return lib
@@ -86,9 +93,11 @@ class RequestState:
     """State of one request: tables, stamps, device-buffer model and length."""
 
     def __init__(self, C: int, S: int, T: int, R: int, length: Optional[int] = None, lib=None,
-                 policy: int = POLICY_LRU, sliding: bool = False):
+                 policy: int = POLICY_LRU, sliding: bool = False, req: int = 0, seed: int = 0):
         self.lib = lib if lib is not None else _lib()
         self.policy = int(policy)
+        # random eviction keys on the request's index and the seed
+        self.req, self.seed = int(req), int(seed) & ((1 << 64) - 1)
         self.sliding = bool(sliding)
         self.C, self.S, self.T, self.R = int(C), int(S), int(T), int(R)
         self.tok_slot = np.empty(C, dtype=np.int32)
@@ -117,7 +126,10 @@ class RequestState:
                 self.stamp.ctypes.data, self.buf.ctypes.data, host.ctypes.data,
                 topk.ctypes.data, int(topk.shape[0]), int(step),
                 out.ctypes.data, counts.ctypes.data)
-        if alias:
+        if self.policy == POLICY_RANDOM:
+            err = self.lib.or_resolve_keyed(*args, self.policy, 1 if self.sliding else 0,
+                                            1 if alias else 0, self.req, self.seed)
+        elif alias:
             err = self.lib.or_resolve_full(*args, self.policy, 1 if self.sliding else 0, 1)
         elif self.sliding:
             err = self.lib.or_resolve_ex(*args, self.policy, 1)
@@ -147,7 +159,8 @@ class RequestState:
 def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.ndarray,
                 length: Optional[int] = None, append_rows: Optional[np.ndarray] = None,
                 tail_init: Optional[Callable[[RequestState], None]] = None,
-                step0: int = 0, policy: int = POLICY_LRU, sliding: bool = False):
+                step0: int = 0, policy: int = POLICY_LRU, sliding: bool = False,
+                req: int = 0, seed: int = 0):
     """Replay ``topk_rows`` [steps][K] for one request from the empty state.
 
     ``append_rows`` [steps][R], when given, is appended before each step's
@@ -155,7 +168,7 @@ def run_request(C: int, S: int, T: int, R: int, host: np.ndarray, topk_rows: np.
     (state, out [steps][K], counts [steps][3], resolve error bits [steps]);
     ``state.append_errs`` holds the OR of the appends' error bits.
     """
-    st = RequestState(C, S, T, R, length, policy=policy, sliding=sliding)
+    st = RequestState(C, S, T, R, length, policy=policy, sliding=sliding, req=req, seed=seed)
     st.append_errs = 0
     if tail_init is not None:
         tail_init(st)

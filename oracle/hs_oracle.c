@@ -25,6 +25,14 @@
  * LRU misses far less).  Besides LRU the oracle offers FIFO, the plainest
  * alternative: a slot's stamp is the step it was filled, hits do not refresh
  * it, and a slot hit in this step is still never evicted in that step.
+ * The third point on that axis is random eviction: the victims are a uniform
+ * random choice among the slots not hit this step, empty slots first.  Each
+ * such slot gets a key, 0 when it is empty and otherwise 1 plus the top 30
+ * bits of one SplitMix64 output (Steele, Lea and Flood, "Fast Splittable
+ * Pseudorandom Number Generators", OOPSLA 2014, with the output function as
+ * Vigna publishes it) of the state seed XOR (step << 32 | request << 14 |
+ * slot); the victims are the slots with the smallest (key, slot) pairs.
+ * Stamps keep the step of last use, as under LRU.
  *
  * Resident tail, two readings of which tokens it holds:
  *   fixed    the last T positions of the capacity, [C - T, C) (a growing
@@ -67,6 +75,7 @@
 
 #define OR_POLICY_LRU 0
 #define OR_POLICY_FIFO 1
+#define OR_POLICY_RANDOM 2
 
 typedef struct {
     int32_t stamp;
@@ -81,6 +90,27 @@ static int or_cmp_pair(const void* a, const void* b)
     if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
     return 0;
 }
+
+/* One SplitMix64 output for the state x: advance by the golden-ratio
+ * increment, then the two xor-shift-multiply rounds and a final xor-shift. */
+static uint64_t or_splitmix64(uint64_t x)
+{
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* Random-eviction key of slot s of request req at step `step`; see the header. */
+static int32_t or_random_key(uint64_t seed, int32_t step, int32_t req, int32_t s, int32_t empty)
+{
+    if (empty) return 0;
+    const uint64_t x = ((uint64_t)(uint32_t)step << 32) | ((uint64_t)(uint32_t)req << 14) | (uint64_t)(uint32_t)s;
+    return 1 + (int32_t)(or_splitmix64(seed ^ x) >> 34);
+}
+
+/* The generator alone, for its known-answer test. */
+uint64_t or_splitmix64_at(uint64_t x) { return or_splitmix64(x); }
 
 static int or_cmp_int(const void* a, const void* b)
 {
@@ -112,11 +142,11 @@ void or_init(int32_t C, int32_t S, int32_t* tok_slot, int32_t* slot_tok, int32_t
  *
  * Returns the error bits (OR_E_*).
  */
-int32_t or_resolve_full(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
-                        int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
-                        const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
-                        int32_t* out, int32_t* counts, int32_t policy, int32_t sliding,
-                        int32_t alias)
+static int32_t or_resolve_core(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                               int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                               const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                               int32_t* out, int32_t* counts, int32_t policy, int32_t sliding,
+                               int32_t alias, int32_t req, uint64_t seed)
 {
     int32_t err = 0;
     int32_t hits = 0, nmiss = 0, inplace = 0;
@@ -162,16 +192,20 @@ int32_t or_resolve_full(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
         }
     }
 
-    /* Under LRU a hit refreshes the slot's entry; under FIFO it does not. */
-    if (policy == OR_POLICY_LRU)
+    /* Under LRU (and random) a hit refreshes the slot's entry; under FIFO it
+     * does not. */
+    if (policy != OR_POLICY_FIFO)
         for (int32_t s = 0; s < S; ++s)
             if (hit[s]) stamp[s] = step;
 
-    /* Step 2: LRU victims among the slots not hit this step. */
+    /* Step 2: victims among the slots not hit this step: the smallest
+     * (stamp, slot) pairs, or (key, slot) pairs under random eviction. */
     int32_t ncand = 0;
     for (int32_t s = 0; s < S; ++s) {
         if (hit[s]) continue;
-        cand[ncand].stamp = stamp[s];
+        cand[ncand].stamp = policy == OR_POLICY_RANDOM
+                                ? or_random_key(seed, step, req, s, slot_tok[s] < 0)
+                                : stamp[s];
         cand[ncand].slot = s;
         ncand += 1;
     }
@@ -210,6 +244,27 @@ int32_t or_resolve_full(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
 
     free(seen); free(first); free(alias_of); free(hit); free(miss_tok); free(miss_pos); free(cand); free(victims);
     return err;
+}
+
+int32_t or_resolve_full(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                        int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                        const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                        int32_t* out, int32_t* counts, int32_t policy, int32_t sliding,
+                        int32_t alias)
+{
+    return or_resolve_core(C, S, T, R, len, tok_slot, slot_tok, stamp, buf, host, topk, K, step,
+                           out, counts, policy, sliding, alias, 0, 0);
+}
+
+/* Any policy, with the request's index and the seed that random eviction keys on. */
+int32_t or_resolve_keyed(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,
+                         int32_t* tok_slot, int32_t* slot_tok, int32_t* stamp, uint8_t* buf,
+                         const uint8_t* host, const int32_t* topk, int32_t K, int32_t step,
+                         int32_t* out, int32_t* counts, int32_t policy, int32_t sliding,
+                         int32_t alias, int32_t req, uint64_t seed)
+{
+    return or_resolve_core(C, S, T, R, len, tok_slot, slot_tok, stamp, buf, host, topk, K, step,
+                           out, counts, policy, sliding, alias, req, seed);
 }
 
 int32_t or_resolve_ex(int32_t C, int32_t S, int32_t T, int32_t R, int32_t len,

@@ -35,7 +35,7 @@ MUTANTS = {
     "tail_offset_from_start": ("out[j] = S + t % T;", "out[j] = S + (t - cold);"),
     "tail_counted_as_miss": ("            inplace += 1;\n", "\n"),
     "stamp_plus_one": ("if (hit[s]) stamp[s] = step;", "if (hit[s]) stamp[s] = step + 1;"),
-    "fifo_refreshes_hits": ("if (policy == OR_POLICY_LRU)\n", "if (1)\n"),
+    "fifo_refreshes_hits": ("if (policy != OR_POLICY_FIFO)\n", "if (1)\n"),
     "sliding_no_write_back": ("if (t >= T) memcpy(host", "if (0) memcpy(host"),
     "sliding_fixed_boundary": ("sliding ? (len - T > 0 ? len - T : 0) : C - T", "C - T"),
     "alias_repeats_unresolved": ("out[j] = out[alias_of[j]];", "out[j] = -1;"),
@@ -82,3 +82,43 @@ def test_pins_reject_planted_mistake(tmp_path, name):
         "sys.exit(0)\n" % (here, os.path.dirname(here), str(so)))
     rc = subprocess.run([sys.executable, "-c", code], capture_output=True).returncode
     assert rc != 0, "planted mistake %s passed every pin" % name
+
+
+# Random eviction: each planted mistake must fail the random-policy pins
+# (tests/test_oracle_random.py: the generator's published outputs, the
+# invariants, the uniform spread, the dependence on request and seed).
+RANDOM_MUTANTS = {
+    "random_key_ignores_request": ("((uint64_t)(uint32_t)req << 14)", "((uint64_t)0 << 14)"),
+    "random_key_ignores_seed": ("or_splitmix64(seed ^ x)", "or_splitmix64(x)"),
+    "random_empty_not_first": ("    if (empty) return 0;\n", "\n"),
+    "random_generator_constant": ("z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;",
+                                  "z = (z ^ (z >> 27)) * 0x94D049BB133111EAull;"),
+    "random_hits_not_refreshed": ("if (policy != OR_POLICY_FIFO)\n", "if (policy == OR_POLICY_LRU)\n"),
+    "random_keys_by_slot": ("return 1 + (int32_t)(or_splitmix64(seed ^ x) >> 34);", "return 1 + s;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RANDOM_MUTANTS))
+def test_random_pins_reject_planted_mistake(tmp_path, name):
+    old, new = RANDOM_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    src = src.replace(old, new)
+    path = tmp_path / ("mut_%s.c" % name)
+    path.write_text(src)
+    so = tmp_path / ("libmut_%s.so" % name)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-w", str(path), "-o", str(so)],
+                   check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import oracle\n"
+        "from test_oracle_random import check_random\n"
+        "lib = oracle.load_library(%r)\n"
+        "try:\n"
+        "    check_random(lib)\n"
+        "except AssertionError:\n"
+        "    sys.exit(3)\n"
+        "sys.exit(0)\n" % (here, os.path.dirname(here), str(so)))
+    rc = subprocess.run([sys.executable, "-c", code], capture_output=True).returncode
+    assert rc != 0, "planted mistake %s passed every random-policy pin" % name
