@@ -460,7 +460,7 @@ def run_ours(args, rank, world, dist):
                         copy_mode=mode)
         stream = torch.cuda.Stream(device=dev)
         try:
-            for pname, pol in (("lru", hs.HS_POLICY_LRU), ("fifo", hs.HS_POLICY_FIFO)):
+            for pname, pol in POLICIES:
                 w.reset()
                 for h in w.handles:
                     hs.hs_set_policy(h.h, pol)
@@ -509,22 +509,22 @@ def run_ours(args, rank, world, dist):
         return out
 
     def miss_curve(base):
-        """Misses per request per step against the buffer size, for both policies: the
+        """Misses per request per step against the buffer size, for each policy: the
         curve behind the blog's miss-count figure (buffer size x eviction policy), on the
         first MISS_CURVE_REQUESTS requests of the workload's trace (the generator keys each
         request's trace by its id, so they are the same requests as in the full run).
         Counting only; the steps are not timed."""
         import numpy as np
         B = min(MISS_CURVE_REQUESTS, base.B)
-        curve = {"requests": B, "steps": args.steps, "buffer_slots": list(MISS_CURVE_SLOTS),
-                 "lru": [], "fifo": []}
+        curve = {"requests": B, "steps": args.steps, "buffer_slots": list(MISS_CURVE_SLOTS)}
+        curve.update({pname: [] for pname, _ in POLICIES})
         stream = torch.cuda.Stream(device=dev)
         for S in MISS_CURVE_SLOTS:
             wl = base.with_(B=B, S=S, host_ratio=-(-base.cold // S))
             w = GpuWorkload(wl, steps=total_steps, record=False, copy_mode=mode)
             try:
                 last = np.zeros(B, dtype=np.int32)
-                for pname, pol in (("lru", hs.HS_POLICY_LRU), ("fifo", hs.HS_POLICY_FIFO)):
+                for pname, pol in POLICIES:
                     w.reset()
                     for h in w.handles:
                         hs.hs_set_policy(h.h, pol)
@@ -541,6 +541,9 @@ def run_ours(args, rank, world, dist):
                 w.close()
         return curve
 
+    # Eviction policies of the sweep and the curve (random eviction keeps the
+    # handles' default seed, 0).
+    POLICIES = (("lru", hs.HS_POLICY_LRU), ("fifo", hs.HS_POLICY_FIFO), ("random", hs.HS_POLICY_RANDOM))
     sweep = {}
     curve = None
     if not args.no_sweep and args.workload == "b64_c64k_s4096":

@@ -40,6 +40,7 @@ struct hs_handle {
     int copy_mode;         // HS_COPY_*
     int cluster_n;         // CTAs per request in cluster mode (1: no cluster fits)
     int policy;            // HS_POLICY_*
+    unsigned long long evict_seed;  // HS_POLICY_RANDOM's seed
     int tail_mode;         // HS_TAIL_*
     int copy_grid;
     int copy_unroll;
@@ -421,6 +422,8 @@ static ResolveArgs resolve_args(const hs_handle* h, const int32_t* topk_idx, int
     ra.rows_per_group = h->copy_rows_per_group;
     ra.done = h->d_done;
     ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
+    ra.random = h->policy == HS_POLICY_RANDOM ? 1 : 0;
+    ra.seed = h->evict_seed;
     ra.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
     ra.alias = alias;
     return ra;
@@ -632,6 +635,8 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
     ra.H = h->H;
     ra.rows_per_group = 1;
     ra.fifo = h->policy == HS_POLICY_FIFO ? 1 : 0;
+    ra.random = h->policy == HS_POLICY_RANDOM ? 1 : 0;
+    ra.seed = h->evict_seed;
     ra.sliding = h->tail_mode == HS_TAIL_SLIDING ? 1 : 0;
     ra.alias = 0;
     if (hs_launch_resolve(ra, h->B, s) != cudaSuccess) return HS_ERR_CUDA;
@@ -740,8 +745,16 @@ int hs_set_tail_mode(hs_handle* h, int mode)
 
 int hs_set_policy(hs_handle* h, int policy)
 {
-    if (!valid(h) || (policy != HS_POLICY_LRU && policy != HS_POLICY_FIFO)) return HS_ERR_ARG;
+    if (!valid(h) || (policy != HS_POLICY_LRU && policy != HS_POLICY_FIFO && policy != HS_POLICY_RANDOM))
+        return HS_ERR_ARG;
     h->policy = policy;
+    return HS_OK;
+}
+
+int hs_set_eviction_seed(hs_handle* h, uint64_t seed)
+{
+    if (!valid(h)) return HS_ERR_ARG;
+    h->evict_seed = seed;
     return HS_OK;
 }
 

@@ -40,6 +40,8 @@ struct ResolveArgs {
     int rows_per_group;
     unsigned* done;        // CTAs finished this call (returns to 0 after each call)
     int fifo;              // 1: FIFO eviction (hits keep their fill stamp), 0: LRU
+    int random;            // 1: random eviction (keys from seed, step, request, slot)
+    unsigned long long seed;  // random eviction's seed
     int sliding;           // 1: the tail is [len - T, len) per request; 0: [C - T, C)
     int alias;             // 1: a repeated token takes its first occurrence's slot (several
                            //    draft positions in one row); 0: a repeat is an error

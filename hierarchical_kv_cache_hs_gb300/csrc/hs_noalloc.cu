@@ -216,6 +216,8 @@ extern "C" int hs_resolve_noalloc(int batch, int ctx_len, int row_bytes, int buf
     ra.rows_per_group = 1;
     ra.done = nullptr;
     ra.fifo = 0;
+    ra.random = 0;
+    ra.seed = 0;
     ra.sliding = 0;
     ra.alias = 0;
     if (hs_launch_resolve(ra, batch, s) != cudaSuccess) return HS_ERR_CUDA;

@@ -75,6 +75,33 @@ static_assert(BPT * NT == NB, "bins per thread");
 
 enum : int { C_NONE = 0, C_BAD = 1, C_TAIL = 2, C_HIT = 3, C_MISS = 4 };
 
+// One SplitMix64 output for the state x (Steele, Lea and Flood, "Fast
+// Splittable Pseudorandom Number Generators", OOPSLA 2014): the state
+// advanced by the golden-ratio increment, two xor-shift-multiply rounds and a
+// final xor-shift.
+__device__ __forceinline__ unsigned long long splitmix64(unsigned long long x)
+{
+    unsigned long long z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// The key that orders slot s for eviction (smallest first).  LRU and FIFO:
+// its stamp.  Random eviction: a slot hit this step (stamp == step) never
+// goes (INT_MAX), an empty slot goes first (0), and any other slot gets 1 +
+// the top 30 bits of SplitMix64 of seed ^ (step << 32 | request << 14 | s).
+__device__ __forceinline__ int evict_key(const ResolveArgs& a, int s, int stamp, int slot_tok,
+                                         int step, int b)
+{
+    if (!a.random) return stamp;
+    if (stamp == step) return INT_MAX;
+    if (slot_tok < 0) return 0;
+    const unsigned long long x = ((unsigned long long)(unsigned)step << 32) |
+                                 ((unsigned long long)(unsigned)b << 14) | (unsigned)s;
+    return 1 + (int)(splitmix64(a.seed ^ x) >> 34);
+}
+
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 {
 #pragma unroll
@@ -609,11 +636,13 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         }
         const int s_pad = (S + NT - 1) / NT * NT;
         int* my_hist = s_hist + (warp % NSUB) * NB;
+        // Random eviction has no age order: every slot counts as "oldest"
+        // (bin 0), so the radix select below runs over the keys.
         for (int i = tid; i < s_pad; i += NT) {
             int bin = NB;
             if (i < S) {
                 const int age = step - s_stamp[i];
-                bin = NB - 1 - (age < NB - 1 ? age : NB - 1);
+                bin = a.random ? 0 : NB - 1 - (age < NB - 1 ? age : NB - 1);
             }
             const unsigned peers = __match_any_sync(FULL, bin);
             if (bin < NB && lane == __ffs(peers) - 1) atomicAdd(&my_hist[bin], __popc(peers));
@@ -649,7 +678,8 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         } else {
             // The m-th oldest slot is among the ages >= NB-1: radix select
             // over the stamps <= lim, most significant digit first.
-            const int lim = step - (NB - 1);
+            // (random eviction: every key below INT_MAX, which marks a hit)
+            const int lim = a.random ? INT_MAX - 1 : step - (NB - 1);
             const int nbits = 32 - __clz(lim > 0 ? lim : 1);
             unsigned prefix = 0, pmask = 0;
             int remaining = m;
@@ -660,7 +690,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
                 for (int i = tid; i < s_pad; i += NT) {
                     int dig = 256;
                     if (i < S) {
-                        const int k = s_stamp[i];
+                        const int k = evict_key(a, i, s_stamp[i], s_slot_tok[i], step, b);
                         if (k <= lim && ((unsigned)k & pmask) == prefix)
                             dig = (int)(((unsigned)k >> shift) & 255u);
                     }
@@ -700,7 +730,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
         const int Q = (S + NT - 1) / NT;
         const int q0 = tid * Q;
         int nl = 0, ne = 0;
-        const bool vec_q = (Q & 3) == 0 && q0 + Q <= S &&  // 16-byte aligned, all in range
+        const bool vec_q = !a.random && (Q & 3) == 0 && q0 + Q <= S &&  // 16-byte aligned, all in range
                            ((uintptr_t)s_stamp & 15u) == 0;
         if (vec_q) {
             for (int q = 0; q < Q; q += 4) {
@@ -712,7 +742,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             for (int q = 0; q < Q; ++q) {
                 const int s = q0 + q;
                 if (s < S) {
-                    const int k = s_stamp[s];
+                    const int k = evict_key(a, s, s_stamp[s], s_slot_tok[s], step, b);
                     nl += k < tau;
                     ne += k == tau;
                 }
@@ -745,7 +775,7 @@ __device__ __forceinline__ void resolve_cta(const ResolveArgs& a, const int b,
             } else {
                 for (int q = 0; q < Q; ++q) {
                     const int s = q0 + q;
-                    if (s < S) place(s, s_stamp[s]);
+                    if (s < S) place(s, evict_key(a, s, s_stamp[s], s_slot_tok[s], step, b));
                 }
             }
         }

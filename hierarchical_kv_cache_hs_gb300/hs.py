@@ -37,6 +37,7 @@ HS_TAIL_SLIDING = 1
 
 HS_POLICY_LRU = 0
 HS_POLICY_FIFO = 1
+HS_POLICY_RANDOM = 2
 
 HS_COPY_AUTO = 0
 HS_COPY_FUSED = 1
@@ -116,6 +117,7 @@ def _load():
         "hs_launch_mode": ([P], I),
         "hs_resolve_launches": ([P], I),
         "hs_set_policy": ([P, I], I),
+        "hs_set_eviction_seed": ([P, ctypes.c_uint64], I),
         "hs_set_tail_mode": ([P, I], I),
         "hs_resolve_noalloc": ([I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, P, P], I),
         "hs_error_string": ([I], ctypes.c_char_p),
@@ -421,6 +423,11 @@ def hs_set_tail_mode(h: int, mode: int) -> None:
 
 def hs_set_policy(h: int, policy: int) -> None:
     _check(lib.hs_set_policy(h, int(policy)), "hs_set_policy")
+
+
+def hs_set_eviction_seed(h: int, seed: int) -> None:
+    """Seed of HS_POLICY_RANDOM's keys (64 bits)."""
+    _check(lib.hs_set_eviction_seed(h, int(seed) & ((1 << 64) - 1)), "hs_set_eviction_seed")
 
 
 def hs_resolve_launches(h: int) -> int:

@@ -435,15 +435,26 @@ int hs_set_copy_mode(hs_handle* h, int mode);
  *                   refreshes its slot's stamp (default);
  *   HS_POLICY_FIFO  victims are the slots filled longest ago; a hit keeps its
  *                   slot's fill stamp (the slot is still not evicted in the
- *                   step that hits it).
- * Ties go to the lowest slot index under both.  Takes effect at the next
- * hs_resolve; switching mid-run keeps the stamps as they are.
+ *                   step that hits it);
+ *   HS_POLICY_RANDOM  victims are a uniform random choice among the slots not
+ *                   hit this step, empty slots first: each slot gets a key, 0
+ *                   when empty, else 1 + the top 30 bits of one SplitMix64
+ *                   output (Steele, Lea and Flood, OOPSLA 2014) of the state
+ *                   seed XOR (step << 32 | request << 14 | slot), and the
+ *                   victims are the smallest (key, slot) pairs; stamps keep
+ *                   the step of last use, as under LRU.  The seed is set with
+ *                   hs_set_eviction_seed (default 0).
+ * Ties go to the lowest slot index under all three.  Takes effect at the next
+ * hs_resolve; switching mid-run keeps the stamps as they are.  The
+ * allocation-free entry point runs LRU only.
  * Source: HiSparse blog, "効率的なSwap-inカーネル"; papercache summary,
  * section 2 "方法细节" (the eviction strategy is one axis of the miss count).
  */
 #define HS_POLICY_LRU   0
 #define HS_POLICY_FIFO  1
+#define HS_POLICY_RANDOM 2
 int hs_set_policy(hs_handle* h, int policy);
+int hs_set_eviction_seed(hs_handle* h, uint64_t seed);
 
 /*
  * Which tokens the resident tail holds (vLLM Hybrid HiSparse post, "Mixed

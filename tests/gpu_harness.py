@@ -33,10 +33,11 @@ def set_cluster_size(h, n):
 
 def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS_COPY_AUTO,
             policy=hs.HS_POLICY_LRU, copy_engine=False, layer_streams=False, one_launch=False,
-            cluster_size=0):
+            cluster_size=0, seed=0):
     """Run ``steps`` steps; ``trace`` [layers][steps][B][K] replaces the generated one.
 
-    ``policy`` is one eviction policy for every layer, or a list with one per layer.
+    ``policy`` is one eviction policy for every layer, or a list with one per layer;
+    ``seed`` is random eviction's seed (layer l's handle takes seed + l).
     ``cluster_size``: CTAs per request in cluster mode (0 = the handle's default)."""
     w = GpuWorkload(wl, steps=steps, record=True, copy_mode=copy_mode)
     if cluster_size:
@@ -44,6 +45,7 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
             set_cluster_size(h.h, cluster_size)
     for layer, h in enumerate(w.handles):
         hs.hs_set_policy(h.h, policy[layer] if isinstance(policy, (list, tuple)) else policy)
+        hs.hs_set_eviction_seed(h.h, seed + layer)
     res_policy = policy
     if setup is not None:
         setup(w)
@@ -85,10 +87,11 @@ def gpu_run(wl, steps=None, trace=None, graph=False, setup=None, copy_mode=hs.HS
     res.state = [h.export_state() for h in w.handles]
     res.workload = w
     res.policy = res_policy
+    res.seed = seed
     return res
 
 
-def oracle_request(wl, layer, b, trace_lb, steps, policy=0):
+def oracle_request(wl, layer, b, trace_lb, steps, policy=0, seed=0):
     host = tg.rows(wl, layer, b, 0, wl.cold)
     append_rows = tg.rows(wl, layer, b, wl.len0, steps) if wl.grow else None
     tail_init = None
@@ -104,7 +107,7 @@ def oracle_request(wl, layer, b, trace_lb, steps, policy=0):
     length = wl.len0 if (wl.grow or wl.sliding) else wl.C
     st, outs, counts, errs = oracle.run_request(
         wl.C, wl.S, wl.T, wl.row_bytes, host, trace_lb, length=length, append_rows=append_rows,
-        tail_init=tail_init, policy=policy, sliding=wl.sliding)
+        tail_init=tail_init, policy=policy, sliding=wl.sliding, req=b, seed=seed)
     st.host_rows = host
     return st, outs, counts, errs
 
@@ -123,7 +126,7 @@ def compare(wl, res, requests=None, layers=None):
         if isinstance(policy, (list, tuple)):
             policy = policy[layer]
         st, outs, counts, errs = oracle_request(wl, layer, b, res.trace[layer, :, b], steps,
-                                                policy=policy)
+                                                policy=policy, seed=getattr(res, "seed", 0) + layer)
         tok, slot_tok, stamp, step = res.state[layer]
         ctx = "layer %d request %d" % (layer, b)
         np.testing.assert_array_equal(res.out[layer, :, b], outs, err_msg=ctx + " out_slot")

@@ -28,10 +28,10 @@ def _built():
 
 
 def _run_and_compare(wl, steps=None, requests=None, graph=False, trace=None, expect_err=0,
-                     copy_mode=0, policy=0, cluster_size=0):
+                     copy_mode=0, policy=0, cluster_size=0, seed=0):
     from gpu_harness import check_counters, compare, gpu_run
     res = gpu_run(wl, steps=steps, graph=graph, trace=trace, copy_mode=copy_mode, policy=policy,
-                  cluster_size=cluster_size)
+                  cluster_size=cluster_size, seed=seed)
     try:
         tot, err = compare(wl, res, requests=requests)
         if requests is None:
@@ -779,6 +779,41 @@ def test_parity_fifo_policy(name, mode):
     """FIFO eviction (hits keep their fill stamp) against the oracle's FIFO."""
     wl = tg.WORKLOADS.get(name) or EDGE[name]
     res, tot = _run_and_compare(wl, copy_mode=mode, policy=1)
+
+
+@pytest.mark.parametrize("name,mode", [("b32_c32k_s4096", 0), ("b32_c32k_s4096", 1),
+                                       ("b32_c32k_s4096", 2), ("tiny_b1_c8k", 0),
+                                       ("b256_c32k_grow_tail512", 0), ("ragged", 3), ("odd_k", 1),
+                                       ("odd_k", 2), ("odd_k", 3), ("single_slot", 0), ("k_equals_s", 3),
+                                       ("max_sizes", 3), ("small_rows", 2)])
+def test_parity_random_policy(name, mode):
+    """Random eviction (keys from SplitMix64 of seed, step, request and slot)
+    against the oracle's, in every launch mode."""
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    _run_and_compare(wl, copy_mode=mode, policy=2, seed=0x5EED0000ABCD + len(name))
+
+
+def test_parity_random_policy_sliding_graph_layers():
+    """Random eviction with a sliding tail, replayed from one CUDA graph, and
+    in the several-layer launch (each layer its own seed)."""
+    from gpu_harness import compare, gpu_run
+    _run_and_compare(SLIDE, copy_mode=3, policy=2, seed=99)
+    _run_and_compare(SLIDE, steps=48, graph=True, requests=[0, 7, 15], policy=2, seed=7)
+    wl = tg.WORKLOADS["b64_c128k_l4_tail4096"]
+    res = gpu_run(wl, steps=24, one_launch=True, policy=[2, 0, 2, 1], seed=1 << 40)
+    try:
+        compare(wl, res, requests=[0, 33, 63])
+    finally:
+        res.workload.close()
+
+
+def test_random_misses_more_than_lru():
+    wl = tg.WORKLOADS["b32_c32k_s4096"]
+    per = {}
+    for policy in (0, 2):
+        res, tot = _run_and_compare(wl, steps=40, policy=policy, seed=3)
+        per[policy] = tot[1]
+    assert per[0] < per[2]
 
 
 def test_fifo_misses_more_than_lru():
