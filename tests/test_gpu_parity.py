@@ -326,6 +326,28 @@ def test_parity_random_workloads(seed):
         res.workload.close()
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_parity_random_workloads_random_eviction(seed):
+    """The random workloads with random eviction on most layers (each layer its
+    own seed), in a random launch mode, every request of every layer against
+    the oracle."""
+    import random
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = _random_workload(2000 + seed)
+    rng = random.Random(3000 + seed)
+    mode = rng.choice([0, 1, 2, 3])
+    policies = [rng.choice([2, 2, 2, 0, 1]) for _ in range(wl.layers)]
+    one = wl.layers > 1 and mode != 3 and rng.random() < 0.5
+    expect = hs.HS_E_APPEND if (wl.grow and not wl.sliding and wl.steps > wl.T) else 0
+    res = gpu_run(wl, copy_mode=mode, policy=policies, one_launch=one, seed=rng.getrandbits(64))
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err | expect)
+    finally:
+        res.workload.close()
+
+
 @pytest.mark.parametrize("seed", range(32))
 def test_parity_random_workloads_cluster(seed):
     """The random workloads in cluster mode with a random cluster size (0 is
