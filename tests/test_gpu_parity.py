@@ -860,8 +860,9 @@ def test_parity_copy_engine_variant(name):
         res.workload.close()
 
 
+@pytest.mark.parametrize("policy", [0, 2], ids=["lru", "random"])
 @pytest.mark.parametrize("mode", [1, 2, 3], ids=["fused", "split", "cluster"])
-def test_parity_multi_position(mode):
+def test_parity_multi_position(mode, policy):
     """Two draft positions per step: the second row repeats about half of the
     first's tokens; repeats share their first occurrence's slot."""
     import oracle
@@ -879,6 +880,8 @@ def test_parity_multi_position(mode):
     h = hs.Handle(B, C, R, S, 8, 0)
     try:
         hs.hs_set_copy_mode(h.h, mode)
+        hs.hs_set_policy(h.h, policy)
+        hs.hs_set_eviction_seed(h.h, 41)
         pool = h.host_pool()
         for b in range(B):
             pool[b, :C] = tg.rows(wl, 0, b, 0, C)
@@ -892,7 +895,7 @@ def test_parity_multi_position(mode):
         stats = h.stats()
         tot_m = 0
         for b in range(B):
-            st = oracle.RequestState(C, S, 0, R)
+            st = oracle.RequestState(C, S, 0, R, policy=policy, req=b, seed=41)
             host = pool[b, :C].copy()
             for s in range(wl.steps):
                 o, c, e = st.resolve(host, trace[s, b], s + 1, alias=True)
