@@ -73,6 +73,8 @@ def test_null_handle_is_rejected(hs):
     assert hs.lib.hs_h2d_read(1, 1, 15, 0, None) == hs.HS_ERR_ARG
     assert hs.lib.hs_reset_requests(None, None, 0, None, None) == hs.HS_ERR_ARG
     assert hs.lib.hs_resolve_layers_host(None, 1, None, 4, None, None) == hs.HS_ERR_ARG
+    assert hs.lib.hs_set_policy(None, hs.HS_POLICY_RANDOM) == hs.HS_ERR_ARG
+    assert hs.lib.hs_set_eviction_seed(None, 1) == hs.HS_ERR_ARG
     hs.hs_destroy(None)  # no-op
 
 
