@@ -28,8 +28,11 @@
  *   rest   = K - carry - zipf draws from the third component: Zipf again,
  *            uniform over [0, n), or uniform over the recent window
  *            [n - W, n).
- * A draw that repeats an index already in the row is redrawn.  The finished
- * row is shuffled with Fisher-Yates so that its order carries no structure.
+ * A draw that repeats an index already in the row is redrawn.  After
+ * TG_MAX_DRAWS_PER_INDEX repeats for one index (a row that takes nearly every
+ * position) the next free position after the last draw is taken instead,
+ * cyclically within the component's range.  The finished row is shuffled with
+ * Fisher-Yates so that its order carries no structure.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -139,6 +142,23 @@ int32_t tg_len_at(const tg_params* p, int32_t s)
 #define TG_MAX_DRAWS_PER_INDEX 100000
 
 /*
+ * The first position in [lo, hi) not taken at this epoch, searching cyclically
+ * from `from`; -1 when every one is taken.  Used only once a component's
+ * random draws have hit TG_MAX_DRAWS_PER_INDEX (a row that takes nearly every
+ * position), so rows that the draws alone can fill are unchanged.
+ */
+static int32_t tg_next_free(const uint32_t* mark, uint32_t epoch, int32_t lo, int32_t hi,
+                            int32_t from)
+{
+    int32_t q = (from >= lo && from < hi) ? from : lo;
+    for (int32_t k = lo; k < hi; ++k) {
+        if (mark[q] != epoch) return q;
+        q = (q + 1 == hi) ? lo : q + 1;
+    }
+    return -1;
+}
+
+/*
  * Rows of steps [0, nsteps) of one (layer, request).  out + s * step_stride
  * receives step s's K indices.  cdf must cover max length over the steps.
  * Returns 0, or -1 on bad arguments / a component that cannot be filled.
@@ -191,24 +211,33 @@ int tg_trace_request(const tg_params* p, const double* cdf, int32_t cdf_n,
             for (;;) {
                 int32_t pos = tg_zipf_pick(cdf, n, tg_unit(&st) * total);
                 if (mark[pos] != epoch) { mark[pos] = epoch; row[cnt++] = pos; ++got; break; }
-                if (++tries > TG_MAX_DRAWS_PER_INDEX) { rc = -1; break; }
+                if (++tries > TG_MAX_DRAWS_PER_INDEX) {
+                    pos = tg_next_free(mark, epoch, 0, n, pos);
+                    if (pos < 0) { rc = -1; break; }
+                    mark[pos] = epoch; row[cnt++] = pos; ++got; break;
+                }
             }
         }
         /* Third component. */
         for (int32_t got = 0; got < rest_q && rc == 0; ) {
             int64_t tries = 0;
             for (;;) {
-                int32_t pos;
+                int32_t pos, lo = 0;
                 if (p->third == TG_THIRD_ZIPF) {
                     pos = tg_zipf_pick(cdf, n, tg_unit(&st) * total);
                 } else if (p->third == TG_THIRD_UNIFORM) {
                     pos = (int32_t)tg_below(&st, n);
                 } else {
                     int32_t w = p->recent < n ? p->recent : n;
-                    pos = n - w + (int32_t)tg_below(&st, w);
+                    lo = n - w;
+                    pos = lo + (int32_t)tg_below(&st, w);
                 }
                 if (mark[pos] != epoch) { mark[pos] = epoch; row[cnt++] = pos; ++got; break; }
-                if (++tries > TG_MAX_DRAWS_PER_INDEX) { rc = -1; break; }
+                if (++tries > TG_MAX_DRAWS_PER_INDEX) {
+                    pos = tg_next_free(mark, epoch, lo, n, pos);
+                    if (pos < 0) { rc = -1; break; }
+                    mark[pos] = epoch; row[cnt++] = pos; ++got; break;
+                }
             }
         }
         /* Fisher-Yates shuffle of the finished row. */

@@ -64,3 +64,24 @@ def test_row_bytes_keyed_by_token(tracegen):
     # roughly uniform bits
     big = tracegen.rows(wl, 0, 0, 0, 512)
     assert abs(np.unpackbits(big).mean() - 0.5) < 0.01
+
+
+@pytest.mark.parametrize("third", ["zipf", "recent"])
+def test_rows_that_take_nearly_every_position(tracegen, third):
+    """A row of K indices out of K + 1 positions: once the random draws for one
+    index give up, the next free position is taken, so every row is complete,
+    distinct and in range (within the recent window for that component)."""
+    C, K = 4097, 4096
+    kw = dict(third=tracegen.THIRD_ZIPF) if third == "zipf" else dict(third=tracegen.THIRD_RECENT,
+                                                                         recent=K)
+    # zipf: half carried over, the rest Zipf over every position; recent: every
+    # index from the window of the last K positions, which it must fill
+    carry = 50 if third == "zipf" else 0
+    wl = tracegen.Workload("nearly_full", 47, B=2, C=C, K=K, S=K, T=0, host_ratio=1, layers=1,
+                           steps=3, len0=C, grow=0, carry_pct=carry, zipf_pct=0, **kw)
+    tr = tracegen.topk_trace(wl, steps=3, requests=[0, 1])
+    for s in range(3):
+        for i in range(2):
+            row = tr[s, i]
+            assert len(np.unique(row)) == K
+            assert row.min() >= (C - K if third == "recent" else 0) and row.max() < C
