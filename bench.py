@@ -646,6 +646,8 @@ def run_ours(args, rank, world, dist):
                      "steps and the warm-up steps run untimed")
     if args.overlap and rank == 0:
         line["layer_overlap"] = layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev)
+    if args.overlap_compute and rank == 0:
+        line["compute_overlap"] = compute_overlap(args, torch, hs, tg, GpuWorkload, wl)
     if "ce_s" in main:
         ce_value = wl.B * wl.layers * main["ce_steps"] / main["ce_s"]
         line["copy_engine_variant"] = {
@@ -687,6 +689,91 @@ def run_ours(args, rank, world, dist):
             per[name] = entry
         line["configs"] = per
     return line
+
+
+def compute_overlap(args, torch, hs, tg, GpuWorkload, wl):
+    """The swap-in steps beside other work on another stream: bf16 4096^3 GEMMs
+    (cuBLAS, standing in for a model's compute), about as many as take the
+    steps' time.  Per launch setup: the steps alone, the GEMMs alone, both at
+    once, and the share of the shorter one hidden, (alone + alone - both) /
+    min(alone, alone).  One layer; the L2 is not flushed here."""
+    prime, n = PRIME_STEPS, 30
+    wl = wl.with_(layers=1)
+    w = GpuWorkload(wl, steps=prime + n)
+    a = torch.randn(4096, 4096, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty_like(a)
+    sa, sb, main = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.current_stream()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def gemms(g, stream):
+        with torch.cuda.stream(stream):
+            for _ in range(g):
+                torch.matmul(a, a, out=c)
+
+    def prime_steps():
+        w.reset()
+        with torch.cuda.stream(sb):
+            for s in range(prime):
+                w.launch_step(s, sb)
+        torch.cuda.synchronize()
+
+    def steps(stream):
+        with torch.cuda.stream(stream):
+            for s in range(prime, prime + n):
+                w.launch_step(s, stream)
+
+    out = {"workload": _workload_desc(wl), "steps": n,
+           "gemm": "torch.matmul bf16 4096 x 4096 x 4096 on another stream"}
+    try:
+        for _ in range(20):
+            torch.matmul(a, a, out=c)
+        e0, e1 = ev(), ev()
+        e0.record(main)
+        gemms(50, main)
+        e1.record(main)
+        torch.cuda.synchronize()
+        t_one = e0.elapsed_time(e1) / 50
+        g = None
+        for tag, mode, ctas in (("default", hs.HS_COPY_AUTO, 0), ("fused", hs.HS_COPY_FUSED, 0),
+                                ("split_48_copy_ctas", hs.HS_COPY_SPLIT, 48)):
+            for h in w.handles:
+                hs.hs_set_copy_mode(h.h, mode)
+                hs.hs_set_copy_ctas(h.h, ctas)
+            prime_steps()
+            e0, e1 = ev(), ev()
+            e0.record(sb)
+            steps(sb)
+            e1.record(sb)
+            torch.cuda.synchronize()
+            t_swap = e0.elapsed_time(e1)
+            if g is None:
+                g = max(1, int(round(t_swap / t_one)))
+                out["gemms"] = g
+            e0, e1 = ev(), ev()
+            e0.record(sa)
+            gemms(g, sa)
+            e1.record(sa)
+            torch.cuda.synchronize()
+            t_gemm = e0.elapsed_time(e1)
+            prime_steps()
+            e0, e1 = ev(), ev()
+            e0.record(main)
+            sa.wait_stream(main)
+            sb.wait_stream(main)
+            gemms(g, sa)
+            steps(sb)
+            main.wait_stream(sa)
+            main.wait_stream(sb)
+            e1.record(main)
+            torch.cuda.synchronize()
+            t_both = e0.elapsed_time(e1)
+            out[tag] = {"swapin_ms": t_swap, "gemm_ms": t_gemm, "both_ms": t_both,
+                        "hidden": (t_swap + t_gemm - t_both) / min(t_swap, t_gemm)}
+    finally:
+        w.close()
+    return out
 
 
 def layer_overlap(args, torch, hs, tg, GpuWorkload, flush, dev):
@@ -867,6 +954,8 @@ def main():
                          "stream and on one stream per layer")
     ap.add_argument("--copy-mode", choices=["auto", "fused", "split", "cluster"], default="auto",
                     help="launch mode of the step (identical results; see hs_set_copy_mode)")
+    ap.add_argument("--overlap-compute", action="store_true",
+                    help="also time the step beside bf16 GEMMs on another stream, per launch setup")
     ap.add_argument("--pool-pages", choices=["auto", "base", "huge"], default="auto",
                     help="host pool placement (identical results; see hs_set_host_pool_pages)")
     args = ap.parse_args()

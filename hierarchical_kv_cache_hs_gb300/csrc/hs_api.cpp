@@ -42,7 +42,8 @@ struct hs_handle {
     int policy;            // HS_POLICY_*
     unsigned long long evict_seed;  // HS_POLICY_RANDOM's seed
     int tail_mode;         // HS_TAIL_*
-    int copy_grid;
+    int copy_grid;         // the copy kernel's default grid: SMs x its occupancy
+    int copy_ctas;         // hs_set_copy_ctas: the grid in use when > 0
     int copy_unroll;
     int copy_rows_per_group;
     size_t pool_bytes, buf_bytes;
@@ -471,7 +472,7 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
     ca.advance_step = 1;
     ca.flat_src = 0;
     if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
-    if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
+    if (hs_launch_copy(ca, h->copy_ctas > 0 ? h->copy_ctas : h->copy_grid, h->copy_unroll, s, !prof) != cudaSuccess) return HS_ERR_CUDA;
     if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
     return HS_OK;
 }
@@ -700,7 +701,7 @@ int hs_resolve_ce(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slo
     ca.rows_per_group = h->copy_rows_per_group;
     ca.advance_step = 1;
     ca.flat_src = 1;
-    if (hs_launch_copy(ca, h->copy_grid, h->copy_unroll, s, false) != cudaSuccess) return HS_ERR_CUDA;
+    if (hs_launch_copy(ca, h->copy_ctas > 0 ? h->copy_ctas : h->copy_grid, h->copy_unroll, s, false) != cudaSuccess) return HS_ERR_CUDA;
     return HS_OK;
 }
 
@@ -762,6 +763,13 @@ int hs_set_copy_mode(hs_handle* h, int mode)
 {
     if (!valid(h) || mode < HS_COPY_AUTO || mode > HS_COPY_CLUSTER) return HS_ERR_ARG;
     h->copy_mode = mode;
+    return HS_OK;
+}
+
+int hs_set_copy_ctas(hs_handle* h, int n)
+{
+    if (!valid(h) || n < 0 || n > HS_MAX_COPY_CTAS) return HS_ERR_ARG;
+    h->copy_ctas = n;
     return HS_OK;
 }
 

@@ -46,6 +46,7 @@ HS_COPY_CLUSTER = 3
 HS_MAX_CLUSTER = 16
 HS_CLUSTER_WIDE_BATCH = 4
 HS_CLUSTER_MAX_BATCH = 128
+HS_MAX_COPY_CTAS = 65535
 HS_POOL_PAGES_AUTO = 0
 HS_POOL_PAGES_BASE = 1
 HS_POOL_PAGES_HUGE = 2
@@ -113,6 +114,7 @@ def _load():
         "hs_profile_events": ([P, P, P], I),
         "hs_set_copy_mode": ([P, I], I),
         "hs_set_cluster_size": ([P, I], I),
+        "hs_set_copy_ctas": ([P, I], I),
         "hs_cluster_size": ([P], I),
         "hs_launch_mode": ([P], I),
         "hs_resolve_launches": ([P], I),
@@ -395,6 +397,11 @@ def hs_resolve_noalloc(batch, ctx_len, row_bytes, buffer_slots, host_rows, resid
 
 def hs_set_copy_mode(h: int, mode: int) -> None:
     _check(lib.hs_set_copy_mode(h, int(mode)), "hs_set_copy_mode")
+
+
+def hs_set_copy_ctas(h: int, n: int) -> None:
+    """CTAs of the split mode's copy kernel (0 = the default grid)."""
+    _check(lib.hs_set_copy_ctas(h, int(n)), "hs_set_copy_ctas")
 
 
 def hs_set_cluster_size(h: int, n: int) -> None:

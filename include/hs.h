@@ -429,6 +429,24 @@ int hs_h2d_read(const void* src_host, void* dst_dev, size_t bytes, int blocks,
 int hs_set_copy_mode(hs_handle* h, int mode);
 
 /*
+ * CTAs of the split mode's grid-wide copy kernel (HS_COPY_SPLIT, and the
+ * copy-engine variant's scatter): n = 0 (default) launches one per SM times
+ * the kernel's occupancy; 1 <= n <= HS_MAX_COPY_CTAS launches n.  Every n
+ * gives the same results.  A small grid leaves the other SMs to kernels on
+ * other streams while the rows cross the host link, which a few dozen CTAs
+ * keep busy: the overlap of the miss I/O with other work.  When the step runs
+ * beside compute on other streams, HS_COPY_SPLIT with about 48 copy CTAs (or
+ * HS_COPY_FUSED for a small batch) overlaps far better than the default
+ * cluster launch, which takes every SM while it runs.  Returns HS_OK or
+ * HS_ERR_ARG.
+ * Source: HiSparse blog, "今後の展望", and papercache summary, section 4
+ * "结论与未来工作" (overlapping the miss I/O with other work as the way to cut
+ * its overhead).
+ */
+#define HS_MAX_COPY_CTAS 65535
+int hs_set_copy_ctas(hs_handle* h, int n);
+
+/*
  * Eviction policy (HiSparse blog, "Efficient swap-in kernel": the miss count
  * depends on the buffer size and the eviction strategy):
  *   HS_POLICY_LRU   victims are the least recently used slots; a hit

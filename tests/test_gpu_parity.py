@@ -838,6 +838,23 @@ def test_random_misses_more_than_lru():
     assert per[0] < per[2]
 
 
+@pytest.mark.parametrize("name,ctas", [("b32_c32k_s4096", 1), ("b32_c32k_s4096", 48),
+                                       ("odd_k", 3), ("ragged", 7), ("b256_c32k_grow_tail512", 48)])
+def test_parity_split_copy_grid(name, ctas):
+    """The split mode's copy kernel on a small grid (hs_set_copy_ctas): each warp
+    takes a longer run of the flattened miss list, with the same results."""
+    from gpu_harness import check_counters, compare, gpu_run
+    from hierarchical_kv_cache_hs_gb300 import hs
+    wl = tg.WORKLOADS.get(name) or EDGE[name]
+    res = gpu_run(wl, copy_mode=hs.HS_COPY_SPLIT,
+                  setup=lambda w: [hs.hs_set_copy_ctas(h.h, ctas) for h in w.handles])
+    try:
+        tot, err = compare(wl, res)
+        check_counters(wl, res, tot, err)
+    finally:
+        res.workload.close()
+
+
 def test_fifo_misses_more_than_lru():
     wl = tg.WORKLOADS["b32_c32k_s4096"]
     per = {}
