@@ -39,6 +39,9 @@ struct hs_handle {
     cudaEvent_t prof_before, prof_after;  // optional, around the copy kernel
     int copy_mode;         // HS_COPY_*
     int cluster_n;         // CTAs per request in cluster mode (1: no cluster fits)
+    int cluster_host_n;    // the same when the kernel reads the top-k rows from
+                           // host memory (hs_resolve_host): every CTA of a
+                           // cluster reads its request's row across the link
     int policy;            // HS_POLICY_*
     unsigned long long evict_seed;  // HS_POLICY_RANDOM's seed
     int tail_mode;         // HS_TAIL_*
@@ -249,19 +252,34 @@ int launch_kind(const hs_handle* h)
 
 // CTAs per request in cluster mode (measured on GB300, 1-256 requests of
 // 2048-of-4096 slots): 16 up to HS_CLUSTER_WIDE_BATCH requests, when all of
-// their clusters run at once (8 when 16 do not fit), else 4; each size falls
+// their clusters run at once (8 when 16 do not fit), else 5; each size falls
 // back to the next smaller one the device cannot run.  Above 4 requests,
-// clusters of 4 were the fastest at every batch size measured, also past one
-// wave of the SMs: later clusters resolve while earlier ones copy.
+// clusters of 5 were the fastest of 2, 3, 4, 5, 6, 8 and 16 at every batch
+// size measured (up to 3 % ahead of 4), also past one wave of the SMs:
+// later clusters resolve while earlier ones copy.
 int auto_cluster_size(const hs_handle* h)
 {
     const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;
     if (h->B <= HS_CLUSTER_WIDE_BATCH)
         for (int n = HS_MAX_CLUSTER; n > 4; n >>= 1)
             if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= h->B) return n;
-    for (int n = 4; n >= 2; n >>= 1)
+    // Otherwise 5 CTAs per request (measured faster than 4 at every batch
+    // from 8 to 128 requests), or the largest of 4 and 2 that the device runs.
+    for (int n : {5, 4, 2})
         if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) >= 1) return n;
     return 1;
+}
+
+// The default sizes: auto_cluster_size for the device-resident top-k rows,
+// and at most 4 above HS_CLUSTER_WIDE_BATCH requests when the rows are read
+// from host memory.  Each CTA of a cluster reads its request's row across
+// the host link, so a fifth CTA adds B * K * 4 bytes of link traffic per
+// step; measured through hs_resolve_host, clusters of 4 were 1-2.5 % faster
+// than 5 at 32 and 64 requests, where 5 were faster with the rows on the device.
+void set_auto_cluster_size(hs_handle* h)
+{
+    h->cluster_n = auto_cluster_size(h);
+    h->cluster_host_n = (h->B > HS_CLUSTER_WIDE_BATCH && h->cluster_n > 4) ? 4 : h->cluster_n;
 }
 
 }  // namespace
@@ -352,7 +370,7 @@ int hs_create(int batch, int ctx_len, int row_bytes, int buffer_slots, int host_
     h->copy_grid = sms * hs_copy_blocks_per_sm(h->copy_unroll, batch);
     h->copy_rows_per_group = hs_copy_rows_per_group(row_bytes, h->copy_unroll);
     h->copy_mode = HS_COPY_AUTO;
-    h->cluster_n = auto_cluster_size(h);
+    set_auto_cluster_size(h);
     h->policy = HS_POLICY_LRU;
     h->tail_mode = HS_TAIL_FIXED;
     const int rc = fill_start_state(h);
@@ -376,7 +394,7 @@ void hs_destroy(hs_handle* h)
 }
 
 static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
-                        hs_stream_t stream, int alias);
+                        hs_stream_t stream, int alias, bool host_topk = false);
 
 int hs_resolve(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
                hs_stream_t stream)
@@ -431,7 +449,7 @@ static ResolveArgs resolve_args(const hs_handle* h, const int32_t* topk_idx, int
 }
 
 static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_slot,
-                        hs_stream_t stream, int alias)
+                        hs_stream_t stream, int alias, bool host_topk)
 {
     if (!valid(h) || !topk_idx || !out_slot || K <= 0) return HS_ERR_ARG;
     if (K > h->S) return HS_ERR_TOPK_GT_SLOTS;
@@ -447,7 +465,8 @@ static int resolve_impl(hs_handle* h, const int32_t* topk_idx, int K, int32_t* o
         // rows.  The profiling events then bracket the whole step.
         if (prof && cudaEventRecord(h->prof_before, s) != cudaSuccess) return HS_ERR_CUDA;
         const cudaError_t e = kind == HS_COPY_CLUSTER
-            ? hs_launch_swapin_cluster(ra, h->B, h->cluster_n, h->copy_unroll, s)
+            ? hs_launch_swapin_cluster(ra, h->B, host_topk ? h->cluster_host_n : h->cluster_n,
+                                       h->copy_unroll, s)
             : hs_launch_swapin(ra, h->B, h->copy_unroll, s);
         if (e != cudaSuccess) return HS_ERR_CUDA;
         if (prof && cudaEventRecord(h->prof_after, s) != cudaSuccess) return HS_ERR_CUDA;
@@ -722,12 +741,13 @@ int hs_set_cluster_size(hs_handle* h, int n)
     if (n > HS_MAX_CLUSTER) return HS_ERR_LIMIT;
     DeviceGuard g(h->device);
     if (n == 0) {
-        h->cluster_n = auto_cluster_size(h);
+        set_auto_cluster_size(h);
         return HS_OK;
     }
     const int kmax = h->S < HS_MAX_TOPK ? h->S : HS_MAX_TOPK;
     if (hs_cluster_max_active(kmax, h->S, n, h->copy_unroll) < 1) return HS_ERR_LIMIT;
     h->cluster_n = n;
+    h->cluster_host_n = n;
     return HS_OK;
 }
 
@@ -787,8 +807,8 @@ int hs_resolve_host(hs_handle* h, const int32_t* topk_idx, int K, int32_t* out_s
     void* d_out = nullptr;
     if (cudaHostGetDevicePointer(&d_in, const_cast<int32_t*>(topk_idx), 0) == cudaSuccess &&
         cudaHostGetDevicePointer(&d_out, out_slot, 0) == cudaSuccess) {
-        const int rc = hs_resolve(h, static_cast<const int32_t*>(d_in), K,
-                                  static_cast<int32_t*>(d_out), stream);
+        const int rc = resolve_impl(h, static_cast<const int32_t*>(d_in), K,
+                                    static_cast<int32_t*>(d_out), stream, 0, true);
         if (rc != HS_OK) return rc;
         return cudaStreamSynchronize(s) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
     }

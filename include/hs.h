@@ -210,7 +210,10 @@ int hs_resolve_layers_host(hs_handle* const* handles, int L, const int32_t* cons
  * [B][K]) out; synchronises the stream before returning.  When both buffers
  * are page-locked and mapped into the device address space (cudaHostAlloc,
  * cudaMallocHost, or cudaHostRegister with mapping), the kernels read and
- * write them across the host link directly; otherwise they are staged
+ * write them across the host link directly (every CTA of a request's cluster
+ * reads its top-k row, so with the default cluster size this call launches
+ * clusters of at most 4 CTAs above HS_CLUSTER_WIDE_BATCH requests); otherwise
+ * they are staged
  * through device buffers with two cudaMemcpyAsync.  The choice follows
  * cudaHostGetDevicePointer: on a system whose GPU addresses pageable host
  * memory (a Grace host), it can accept ordinary malloc'd buffers too, and
@@ -495,11 +498,12 @@ int hs_set_tail_mode(hs_handle* h, int mode);
 /*
  * CTAs per request in HS_COPY_CLUSTER mode.  n = 0 (the default) picks 16
  * for up to HS_CLUSTER_WIDE_BATCH requests when all of their clusters run at
- * once (else 8 under the same condition), and 4 otherwise (2, then 1, when
- * the device cannot run it); otherwise 2 <= n <= HS_MAX_CLUSTER, refused
+ * once (else 8 under the same condition), and 5 otherwise (4, then 2, then
+ * 1, when the device cannot run it); otherwise 2 <= n <= HS_MAX_CLUSTER, refused
  * (HS_ERR_LIMIT) when the device cannot run clusters of n such CTAs.
  * hs_cluster_size returns the size in use (1 when no cluster size fits: the
- * cluster mode then launches the fused kernel).
+ * cluster mode then launches the fused kernel); hs_resolve_host reading
+ * mapped top-k rows takes at most 4 of the default (see there).
  * Source: no passage (a launch-shape knob of this library).
  */
 int hs_set_cluster_size(hs_handle* h, int n);

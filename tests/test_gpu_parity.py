@@ -1195,7 +1195,7 @@ def test_device_errors_leave_context_usable():
 
 def test_cluster_size_settings():
     """hs_set_cluster_size: 0 picks the default (16 or 8 CTAs up to 4
-    requests, 4 beyond), 2..HS_MAX_CLUSTER are taken when the device runs
+    requests, 5 beyond), 2..HS_MAX_CLUSTER are taken when the device runs
     them, other values are refused; cluster mode is one launch per step."""
     from hierarchical_kv_cache_hs_gb300 import hs
     h = hs.Handle(4, 8192, 1152, 1024, 8)
@@ -1220,7 +1220,7 @@ def test_cluster_size_settings():
         h.close()
     big = hs.Handle(200, 4096, 64, 256, 16)
     try:
-        assert hs.hs_cluster_size(big.h) == 4  # the size cluster mode would take
+        assert hs.hs_cluster_size(big.h) == 5  # the size cluster mode would take
         # beyond HS_CLUSTER_MAX_BATCH requests the default takes one CTA per request
         assert hs.hs_launch_mode(big.h) == hs.HS_COPY_FUSED
         hs.hs_set_copy_mode(big.h, hs.HS_COPY_CLUSTER)
